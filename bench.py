@@ -1,0 +1,412 @@
+"""Benchmark: shifted-window video attention on GB300.
+
+One step = two layers of the alternating schedule on the 1080p-like grid
+(T=21, H=68, W=120; nt=4, nh=nw=3; 24 heads x 128; 256 text tokens; bf16):
+
+    window attention, REGULAR layout   (wp_window_attn: tcgen05 kernel + text mean)
+    re-layout of the hidden rows [N, 2560] REGULAR -> SHIFTED   (wp_permute)
+    window attention, SHIFTED layout
+    re-layout of the hidden rows SHIFTED -> REGULAR
+
+Inputs are synthetic N(0,1) (seeded) and resident in HBM before the timed
+region; every input is larger than L2, so no flush is needed between steps.
+The headline value is attention TFLOP/s over the whole step time (permutes
+included); the kernel-level numbers and the roofline are reported beside it.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload 1080p|720p]
+
+--impl reference times the CPU oracle on the host cores (bounded samples of
+the same workload, same metric and unit).  Under torchrun every rank runs an
+independent replica (the path has nothing to shard); the step time is the
+max over ranks.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "window-attn TFLOP/s (% BF16 peak) and re-layout GB/s (% HBM) at 720p/1080p grids"
+WORKLOADS = {
+    "1080p": dict(T=21, H=68, W=120, nt=4, nh=3, nw=3, heads=24, hd=128, L=256, hidden=2560),
+    "720p": dict(T=21, H=45, W=80, nt=4, nh=3, nw=3, heads=24, hd=128, L=256, hidden=2560),
+}
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 * 1024 * 1024
+
+
+def workload_desc(name, w):
+    return ("%s-like grid T=%d H=%d W=%d (N=%d), nt=%d nh=%d nw=%d, heads=%d head_dim=%d, text L=%d, "
+            "bf16; step = attn(regular) + relayout [N,%d] bf16 regular->shifted + attn(shifted) + "
+            "relayout shifted->regular" % (name, w["T"], w["H"], w["W"], w["T"] * w["H"] * w["W"],
+                                          w["nt"], w["nh"], w["nw"], w["heads"], w["hd"], w["L"],
+                                          w["hidden"]))
+
+
+def attn_flops(win_sizes, heads, hd, L):
+    """4 * heads * hd * sum_w (n_w + L)^2 -- QK^T and PV over real rows only."""
+    s = np.asarray(win_sizes, dtype=np.float64) + L
+    return 4.0 * heads * hd * float((s * s).sum())
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def recorded_traffic(kernel_file, key):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current source of the kernel (sha256 match); else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    src = os.path.join(ROOT, "video_dit_shifted_gb300", "csrc", kernel_file)
+    if not os.path.exists(path) or not os.path.exists(src):
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    for line in open(path):
+        f = line.split()
+        if len(f) >= 3 and not line.startswith("#") and f[0] == key and f[1] == sha:
+            return float(f[2])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index, self.proc = index, None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = []
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) == 7:
+                rows.append(f)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[3 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": float(rows[0][1]) if rows[0][1].replace(".", "").isdigit() else None,
+                "power_w_max": max(float(r[2]) for r in rows if r[2].replace(".", "").isdigit()),
+                "samples": len(rows), "reasons": reasons}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+        pg = dist
+    return world, rank, local, pg
+
+
+def barrier(pg):
+    if pg is not None:
+        pg.barrier()
+
+
+def max_over_ranks(pg, x, device):
+    if pg is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return t.item()
+
+
+# ------------------------------------------------------------------ ours --
+class Workload:
+    def __init__(self, name, device):
+        import video_dit_shifted_gb300 as vds
+        from video_dit_shifted_gb300 import synth
+        self.vds, self.w, self.name, self.dev = vds, WORKLOADS[name], name, device
+        w = self.w
+        self.plan = vds.Plan(w["T"], w["H"], w["W"], w["nt"], w["nh"], w["nw"], device=device)
+        N, heads, hd, L = self.plan.N, w["heads"], w["hd"], w["L"]
+        self.N = N
+        x = synth.attention_inputs(N, L, heads, hd, torch.bfloat16, device)
+        self.qkv = {vds.REGULAR: x["vid_buf"], vds.SHIFTED: torch.empty_like(x["vid_buf"])}
+        vds.permute(self.plan, x["vid_buf"].view(N, -1), self.qkv[vds.SHIFTED].view(N, -1),
+                    vds.REGULAR, vds.SHIFTED)
+        self.txt = x["txt_buf"]
+        self.hidden = synth.hidden(N, w["hidden"], torch.bfloat16, device)
+        self.hidden2 = torch.empty_like(self.hidden)
+        self.o_vid = {l: torch.empty((N, heads, hd), dtype=torch.bfloat16, device=device)
+                      for l in (vds.REGULAR, vds.SHIFTED)}
+        self.o_txt = {l: torch.empty((L, heads, hd), dtype=torch.bfloat16, device=device)
+                      for l in (vds.REGULAR, vds.SHIFTED)}
+        self.ws = {l: vds.make_workspace(self.plan, l, heads, hd, L, vds.BF16, device)
+                   for l in (vds.REGULAR, vds.SHIFTED)}
+        self.flops = {}
+        for l in (vds.REGULAR, vds.SHIFTED):
+            off = self.plan.host_tables(l)[0]
+            self.flops[l] = attn_flops(np.diff(off), heads, hd, L)
+        self.relayout_bytes = 2.0 * N * w["hidden"] * 2  # read + write per re-layout
+        torch.cuda.synchronize()
+
+    def attn(self, layout):
+        vds, t = self.vds, self.txt
+        b = self.qkv[layout]
+        vds.window_attn(self.plan, layout, b[:, 0], b[:, 1], b[:, 2], t[:, 0], t[:, 1], t[:, 2],
+                        self.o_vid[layout], self.o_txt[layout], self.ws[layout])
+
+    def step(self, ev=None):
+        """ev: list of 8 events to bracket the four launches (or None)."""
+        vds = self.vds
+        rec = (lambda i: ev[i].record()) if ev else (lambda i: None)
+        rec(0); self.attn(vds.REGULAR); rec(1)
+        rec(2); vds.permute(self.plan, self.hidden, self.hidden2, vds.REGULAR, vds.SHIFTED); rec(3)
+        rec(4); self.attn(vds.SHIFTED); rec(5)
+        rec(6); vds.permute(self.plan, self.hidden2, self.hidden, vds.SHIFTED, vds.REGULAR); rec(7)
+
+    launches_per_step = 6  # 2 x (attention kernel + text mean) + 2 x permute
+
+    def step_flops(self):
+        return self.flops[self.vds.REGULAR] + self.flops[self.vds.SHIFTED]
+
+    def check_status(self):
+        for l, ws in self.ws.items():
+            st = self.vds.read_status(ws)
+            if st != 0:
+                raise RuntimeError("device status %d after layout %d" % (st, l))
+
+
+def run_e2e(wl, steps, warmup):
+    """Same step through the public API, with every input copied in from
+    pinned host memory and every output copied back, inside the timing."""
+    vds = wl.vds
+    host_in = {"qkv_reg": wl.qkv[vds.REGULAR], "qkv_shf": wl.qkv[vds.SHIFTED], "txt": wl.txt,
+               "hidden": wl.hidden}
+    pinned_in = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in host_in.items()}
+    for k in pinned_in:
+        pinned_in[k].copy_(host_in[k])
+    outs = [wl.o_vid[vds.REGULAR], wl.o_vid[vds.SHIFTED], wl.o_txt[vds.REGULAR], wl.o_txt[vds.SHIFTED],
+            wl.hidden]
+    pinned_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    h2d = sum(t.numel() * t.element_size() for t in pinned_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in pinned_out)
+    dev_in = {"qkv_reg": wl.qkv[vds.REGULAR], "qkv_shf": wl.qkv[vds.SHIFTED], "txt": wl.txt,
+              "hidden": wl.hidden}
+
+    def one():
+        for k in pinned_in:
+            dev_in[k].copy_(pinned_in[k], non_blocking=True)
+        wl.step()
+        for o, p in zip(outs, pinned_out):
+            p.copy_(o, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        one()
+    e.record()
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) / steps, h2d, d2h
+
+
+def oracle_sample(wl_name, budget_s, seed_rows=None):
+    """Time the CPU oracle on (window, head) pairs of the REGULAR layer, in
+    window order, until budget_s seconds of work.  Inputs are synthetic
+    N(0,1) float values drawn on the host (the oracle's cost does not depend
+    on the values).  Returns (tflops, pairs, flops, seconds)."""
+    from oracle import attention as oa
+    from oracle import plan as op
+    w = WORKLOADS[wl_name]
+    off, ids = op.layout_tables(w["T"], w["H"], w["W"], w["nt"], w["nh"], w["nw"], op.REGULAR)
+    rng = np.random.default_rng(0)
+    heads, hd, L = w["heads"], w["hd"], w["L"]
+    txt = [rng.standard_normal((L, 1, hd)) for _ in range(3)]
+    done, flops, t_used = 0, 0.0, 0.0
+    nwin = len(off) - 1
+    k = 0
+    while t_used < budget_s and k < nwin * heads:
+        win = k % nwin
+        n_w = int(off[win + 1] - off[win])
+        q, kk, v = (rng.standard_normal((n_w, 1, hd)) for _ in range(3))
+        sub_off = np.array([0, n_w])
+        t0 = time.perf_counter()
+        oa.window_attention(q, kk, v, *txt, sub_off, np.arange(n_w))
+        t_used += time.perf_counter() - t0
+        flops += attn_flops([n_w], 1, hd, L)
+        done += 1
+        k += 1
+    return flops / t_used / 1e12, done, flops, t_used
+
+
+def host_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [d.get("num_threads") for d in threadpool_info() if d.get("internal_api") in ("openblas", "mkl")]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return len(os.sched_getaffinity(0))
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = WORKLOADS[args.workload]
+    times, flops_all = [], []
+    for i in range(args.warmup + args.steps):
+        tf, pairs, fl, secs = oracle_sample(args.workload, args.ref_step_s)
+        if i >= args.warmup:
+            times.append(secs)
+            flops_all.append(fl)
+    val = sum(flops_all) / sum(times) / 1e12
+    cores = host_threads()
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": workload_desc(args.workload, w)},
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": "per step: (window, head) pairs of the regular layer in window order "
+                                       "until %.0f s of float64 oracle work" % args.ref_step_s},
+            "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    world, rank, local, pg = dist_setup(args)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+    __graft_entry__.build()
+    wl = Workload(args.workload, dev)
+    vds = wl.vds
+    for _ in range(args.warmup):
+        wl.step()
+    torch.cuda.synchronize()
+    wl.check_status()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(args.steps)]
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(dev.index if world == 1 else local)
+    clocks.start()
+    barrier(pg)
+    torch.cuda.synchronize()
+    s.record()
+    for i in range(args.steps):
+        wl.step(evs[i])
+    e.record()
+    torch.cuda.synchronize()
+    barrier(pg)
+    clk = clocks.stop()
+    wl.check_status()
+    total_ms = max_over_ranks(pg, s.elapsed_time(e), dev)
+    ms_step = total_ms / args.steps
+    attn_reg = [ev[0].elapsed_time(ev[1]) for ev in evs]
+    attn_shf = [ev[4].elapsed_time(ev[5]) for ev in evs]
+    perm = [ev[2].elapsed_time(ev[3]) for ev in evs] + [ev[6].elapsed_time(ev[7]) for ev in evs]
+    f_reg, f_shf = wl.flops[vds.REGULAR], wl.flops[vds.SHIFTED]
+    step_flops = f_reg + f_shf
+    value = world * step_flops / (ms_step * 1e-3) / 1e12
+    attn_ms = (sum(attn_reg) + sum(attn_shf)) / (2 * args.steps)
+    attn_tflops = (f_reg + f_shf) / 2 / (attn_ms * 1e-3) / 1e12
+    perm_ms = sum(perm) / len(perm)
+    relayout_gbs = wl.relayout_bytes / (perm_ms * 1e-3) / 1e9
+    peaks, peak_src = load_peaks()
+    traffic = recorded_traffic("attn_tc.cu", "attn_tc_1080p") if args.workload == "1080p" else None
+    roofline = {"bound": "tensor", "achieved": attn_tflops, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": attn_tflops / peaks["bf16_tflops"], "traffic": traffic,
+                "peak_source": peak_src + " (bf16 burst)",
+                "kernel": "attn_tc_kernel (+ text_mean_kernel inside the same timed call)",
+                "frac_of_sustained": attn_tflops / peaks["bf16_tflops_sustained"],
+                "per_layout_ms": {"regular": sum(attn_reg) / args.steps, "shifted": sum(attn_shf) / args.steps},
+                "flops_per_launch": {"regular": f_reg, "shifted": f_shf}}
+    relayout = {"bound": "hbm", "achieved": relayout_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": relayout_gbs / peaks["hbm_gbs"],
+                "traffic": recorded_traffic("permute.cu", "permute_1080p") if args.workload == "1080p" else None,
+                "kernel": "permute_rows_kernel", "bytes_per_launch": wl.relayout_bytes, "ms": perm_ms,
+                "peak_source": peak_src}
+    e2e_ms, h2d, d2h = run_e2e(wl, args.e2e_steps, max(1, min(args.warmup, 2)))
+    e2e_ms = max_over_ranks(pg, e2e_ms, dev)
+    e2e = {"value": world * step_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+           "steps": args.e2e_steps}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tf, pairs, fl, secs = oracle_sample(args.workload, args.cpu_budget_s)
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": host_threads(), "kind": "oracle",
+               "sample": "%d (window, head) pairs of the regular layer (%.1f GFLOP, %.1f s), float64 numpy"
+                         % (pairs, fl / 1e9, secs)}
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": workload_desc(args.workload, wl.w),
+                           "l2": "inputs larger than L2 (qkv %.2f GB, hidden %.2f GB): no flush"
+                                 % (wl.qkv[vds.REGULAR].numel() * 2 / 1e9, wl.hidden.numel() * 2 / 1e9),
+                           "parallelism": "replicas" if world > 1 else "single GPU"},
+                "attn_tflops": attn_tflops, "relayout_gbs": relayout_gbs,
+                "roofline": roofline, "roofline_relayout": relayout, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": wl.launches_per_step * args.steps, "clocks": clk}
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="1080p")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    ap.add_argument("--ref-step-s", type=float, default=4.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        print("note: --warmup raised to 3 (timing rules)", file=sys.stderr)
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,179 @@
+/*
+ * wp.h -- C ABI of libwp: shifted-window video attention on GB300 (sm_103a).
+ *
+ * What it computes is defined on the page "Window-Aligned Sequence
+ * Parallelism (SeedVR2)" (vLLM-Omni design docs):
+ *
+ *   §Window layouts      window size normalised to the 720p latent area,
+ *                        regular and half-window-shifted (clipped) layouts,
+ *                        window enumeration w -> h -> t, row-major (t,h,w)
+ *                        token order inside a window, canonical id
+ *                        (t*H + h)*W + w.
+ *   §Motivation, §Plan A at SP=1 a layout boundary is a local permutation.
+ *   §SeedVR2 integration one packed-varlen attention per
+ *                        [video window ; replicated text] segment; video
+ *                        results return to canonical token order.
+ *   §Text stream         next text state = (sum over windows of the
+ *                        window's text output) / (window count of the
+ *                        current layout).
+ *
+ * Conventions shared by every entry point:
+ *   - Every function validates its arguments on the host first and returns a
+ *     wp_status; on any error nothing is launched and wp_last_error() holds a
+ *     one-line message (thread-local, valid until the next call on the same
+ *     thread).
+ *   - Device pointers are plain CUDA device addresses; the caller owns all
+ *     device memory (the library never allocates device memory).  `stream`
+ *     is a cudaStream_t passed as void* (NULL = legacy default stream).  All
+ *     device work is asynchronous on that stream.
+ *   - Faults detected on the device (a bounded wait that expired, a failed
+ *     bounds check) are written to a status word in the attention workspace
+ *     and read back with wp_read_status(); no kernel traps or spins forever.
+ *   - Batch is 1: a batch of videos is more windows.
+ *   - There is no CPU fallback: without a usable sm_103a device every
+ *     launching call returns WP_ECUDA.
+ */
+#ifndef WP_H_
+#define WP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define WP_ABI_VERSION 1
+
+typedef struct wp_plan wp_plan; /* opaque, host-owned, immutable once uploaded */
+
+enum wp_layout {
+  WP_CANONICAL = 0, /* row-major (t,h,w): row i holds canonical token i      */
+  WP_REGULAR = 1,   /* §Window layouts, regular windows                       */
+  WP_SHIFTED = 2    /* §Window layouts, cuts moved by half a window, clipped  */
+};
+
+enum wp_dtype {
+  WP_BF16 = 0, /* bf16 in/out, fp32 accumulation (tcgen05 tensor cores)       */
+  WP_FP32 = 1  /* fp32 in/out, fp32 arithmetic throughout (parity mode)        */
+};
+
+enum wp_status {
+  WP_OK = 0,
+  WP_EINVAL = 1,       /* bad argument (null pointer, size, layout, range)    */
+  WP_EUNSUPPORTED = 2, /* valid but not supported (head_dim, alignment, ...)  */
+  WP_ECUDA = 3,        /* a CUDA runtime/driver call failed                   */
+  WP_ETIMEOUT = 4,     /* device: a bounded wait expired (status word only)   */
+  WP_EDEVICE = 5,      /* device: a bounds check failed (status word only)    */
+  WP_ENOTREADY = 6     /* plan not uploaded, or uploaded on another device    */
+};
+
+/* ------------------------------------------------------------------ plan --
+ * wp_plan_create -- window geometry for a post-patch token grid (T, H, W)
+ * (§Window layouts):
+ *   scale = sqrt(45*80 / (H*W)) (IEEE double),
+ *   wh = ceil(round(H*scale)/nh), ww = ceil(round(W*scale)/nw) (round: ties
+ *   to even), wt = ceil(min(T, 30)/nt).
+ * Regular intervals per axis are [i*w, min((i+1)*w, n)).  Shifted intervals
+ * cut at floor((2k+1)*w/2) (half window, floored -- a reading: the page does
+ * not say how an odd half is rounded) clipped to [0, n]; an axis a single
+ * window already covers is not shifted.  Windows are enumerated w outermost,
+ * then h, then t.  All host work; no CUDA call.
+ * Errors: WP_EINVAL if any argument < 1, T*H*W >= 2^31, or a window
+ * dimension comes out as 0.  *out is set only on success; free it with
+ * wp_plan_destroy. */
+int wp_plan_create(int T, int H, int W, int nt, int nh, int nw, wp_plan** out);
+void wp_plan_destroy(wp_plan* plan); /* NULL is a no-op */
+
+/* Geometry of one layout.  n_tokens = T*H*W; nwin = window count (1 for
+ * WP_CANONICAL); (wt, wh, ww) = window size; max_tokens = largest window.
+ * Any output pointer may be NULL. */
+int wp_plan_info(const wp_plan* plan, int layout, int64_t* n_tokens, int* nwin,
+                 int* wt, int* wh, int* ww, int* max_tokens);
+
+/* Host copies of a layout's tables (for tests and callers that index rows):
+ *   win_off[nwin+1]  row offset of each window in layout order,
+ *   ids[N]           canonical id of the token at each layout row,
+ *   boxes[nwin*6]    (t0,t1,h0,h1,w0,w1) half-open box of each window.
+ * Any output pointer may be NULL. */
+int wp_plan_host_tables(const wp_plan* plan, int layout, int32_t* win_off,
+                        int32_t* ids, int32_t* boxes);
+
+/* Device tables: the caller provides a device buffer of at least
+ * *bytes (wp_plan_device_bytes, 256-byte aligned) and wp_plan_upload copies
+ * every table into it with cudaMemcpyAsync on `stream` from host memory the
+ * plan owns (pageable: the copy is complete when the call returns).  The
+ * plan then refers to that buffer, which must stay alive and unmodified
+ * until the plan is destroyed or uploaded again; it is bound to the current
+ * device.  Tables: per layout win_off, ids and two work-split prefix tables;
+ * the six fused permutation tables perm[a->b][q] = pos_a[ids_b[q]]. */
+int wp_plan_device_bytes(const wp_plan* plan, size_t* bytes);
+int wp_plan_upload(wp_plan* plan, void* dev_buf, size_t bytes, void* stream);
+
+/* --------------------------------------------------------------- permute --
+ * wp_permute -- §Motivation/§Plan A at SP=1: the layout switch as a local row
+ * permutation.  For every destination row q of dst_layout:
+ *     dst[q*dst_stride_B .. +row_B) = src[p*src_stride_B .. +row_B),
+ *     p = row of src_layout that holds canonical token ids_dst[q].
+ * Rows are opaque bytes (any dtype); the copy is exact.  N = T*H*W rows.
+ * src_layout == dst_layout is a strided copy.
+ * Requirements (WP_EUNSUPPORTED otherwise): src, dst 16-byte aligned;
+ * row_B > 0 and a multiple of 16; strides multiples of 16 and >= row_B.
+ * WP_EINVAL: null pointer, bad layout, or the byte ranges of src and dst
+ * overlap (in-place permutation is not supported).  WP_ENOTREADY: plan not
+ * uploaded on the current device. */
+int wp_permute(const wp_plan* plan, int src_layout, int dst_layout,
+               const void* src, int64_t src_stride_B, void* dst,
+               int64_t dst_stride_B, int64_t row_B, void* stream);
+
+/* ------------------------------------------------------------- attention --
+ * wp_attn_workspace_bytes -- device workspace wp_window_attn needs: a
+ * 256-byte status block plus the per-window text outputs
+ * [nwin, L, heads, head_dim] in fp32. */
+int wp_attn_workspace_bytes(const wp_plan* plan, int layout, int heads,
+                            int head_dim, int L, int dtype, size_t* bytes);
+
+/* wp_window_attn -- one layer of window attention (§SeedVR2 integration,
+ * §Text stream) over layout `layout` (WP_REGULAR or WP_SHIFTED).
+ * For every window w and head h, with segment X = [video rows of w ; text]:
+ *     Y = softmax(Q_X K_X^T * s) V_X     (full, no mask; s = softmax_scale,
+ *                                         or 1/sqrt(head_dim) if <= 0)
+ * Video rows of Y are written to o_vid at their CANONICAL row ids; the text
+ * rows of Y are T_w, and o_txt = (T_0 + ... + T_{nwin-1}) / nwin, summed in
+ * window order (deterministic, no atomics).
+ * Layout (element type = dtype):
+ *   q, k, v   [N, heads, head_dim] rows in `layout` order; row r of q starts
+ *             at q + r*vid_row_stride_B (q, k, v share the stride, e.g. a
+ *             packed [N, 3, heads, head_dim] buffer).  Inner dims contiguous.
+ *   qt,kt,vt  [L, heads, head_dim] with row stride txt_row_stride_B.
+ *   o_vid     [N, heads, head_dim], canonical order, row stride
+ *             o_vid_row_stride_B.
+ *   o_txt     [L, heads, head_dim], contiguous.  May be NULL iff L == 0.
+ *   workspace at least wp_attn_workspace_bytes; its status word is cleared
+ *             at the start of the call.
+ * All rows of q/k/v (including rows of neighbouring windows) must be finite.
+ * Supported (WP_EUNSUPPORTED otherwise): head_dim 64 or 128; pointers and
+ * strides multiples of 16 bytes; heads*head_dim*elem <= stride.
+ * WP_EINVAL: null pointer, heads < 1, L < 0, layout not REGULAR/SHIFTED,
+ * workspace too small.  WP_ENOTREADY: plan not uploaded on this device. */
+int wp_window_attn(const wp_plan* plan, int layout, int heads, int head_dim,
+                   int L, int dtype, const void* q, const void* k,
+                   const void* v, int64_t vid_row_stride_B, const void* qt,
+                   const void* kt, const void* vt, int64_t txt_row_stride_B,
+                   void* o_vid, int64_t o_vid_row_stride_B, void* o_txt,
+                   void* workspace, size_t ws_bytes, float softmax_scale,
+                   void* stream);
+
+/* wp_read_status -- copies the device status word of `workspace` to
+ * *device_status (a wp_status value: WP_OK, WP_ETIMEOUT or WP_EDEVICE),
+ * synchronising `stream` first.  Returns WP_ECUDA if the copy fails. */
+int wp_read_status(const void* workspace, int* device_status, void* stream);
+
+/* ---------------------------------------------------------------- misc --- */
+const char* wp_last_error(void); /* never NULL; "" when there is no error */
+int wp_abi_version(void);        /* WP_ABI_VERSION */
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* WP_H_ */

@@ -1,0 +1,154 @@
+"""wp_window_attn on the GPU against the oracle (gpu).
+
+Tolerances: max abs error <= 1e-4 in fp32 mode and <= 2e-2 in bf16 mode,
+against the float64 oracle fed the same input bits.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as oa
+from oracle import plan as op
+
+pytestmark = pytest.mark.gpu
+
+TOL = {torch.float32: 1e-4, torch.bfloat16: 2e-2}
+
+
+@pytest.fixture(scope="module")
+def vds():
+    import __graft_entry__
+    __graft_entry__.build()
+    import video_dit_shifted_gb300 as m
+    return m
+
+
+def _np(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def _run(vds, plan, layout, x, heads, hd, L, dtype, scale=0.0):
+    N = plan.N
+    dev = x["q"].device
+    code = vds.BF16 if dtype == torch.bfloat16 else vds.FP32
+    o_vid = torch.full((N, heads, hd), float("nan"), dtype=dtype, device=dev)
+    o_txt = torch.full((L, heads, hd), float("nan"), dtype=dtype, device=dev)
+    ws = vds.make_workspace(plan, layout, heads, hd, L, code, dev)
+    vds.window_attn(plan, layout, x["q"], x["k"], x["v"], x["qt"], x["kt"], x["vt"], o_vid, o_txt, ws,
+                    scale=scale)
+    assert vds.read_status(ws) == 0
+    return o_vid, o_txt, ws
+
+
+def _check_full(vds, grid, heads, hd, L, dtype, layouts=(op.REGULAR, op.SHIFTED), scale=0.0):
+    from video_dit_shifted_gb300 import synth
+    plan = vds.Plan(*grid, device="cuda")
+    N = plan.N
+    for layout in layouts:
+        x = synth.attention_inputs(N, L, heads, hd, dtype, "cuda", base_seed=10 * layout)
+        o_vid, o_txt, _ = _run(vds, plan, layout, x, heads, hd, L, dtype, scale)
+        off, ids = op.layout_tables(*grid, layout)
+        ref_o, ref_t = oa.window_attention(*(_np(x[n]) for n in ("q", "k", "v", "qt", "kt", "vt")), off, ids,
+                                           scale=scale if scale > 0 else None)
+        err_v = np.abs(_np(o_vid) - ref_o).max()
+        assert err_v <= TOL[dtype], (layout, err_v)
+        if L:
+            err_t = np.abs(_np(o_txt) - oa.text_mean(ref_t)).max()
+            assert err_t <= TOL[dtype], (layout, err_t)
+    plan.close()
+
+
+def test_pr1_fp32(vds):
+    """T=2, H=45, W=80, nt=1, nh=nw=3; heads 2, head_dim 64, L 16, fp32."""
+    _check_full(vds, (2, 45, 80, 1, 3, 3), 2, 64, 16, torch.float32)
+
+
+@pytest.mark.parametrize("hd", [64, 128])
+def test_pr1_grid_bf16(vds, hd):
+    _check_full(vds, (2, 45, 80, 1, 3, 3), 2, hd, 16, torch.bfloat16)
+
+
+@pytest.mark.parametrize("L", [0, 1, 128, 300])
+def test_text_lengths_bf16(vds, L):
+    """No text, one token, exactly one tile, and a ragged third tile."""
+    _check_full(vds, (3, 30, 40, 2, 3, 3), 2, 128, L, torch.bfloat16)
+
+
+@pytest.mark.parametrize("L", [0, 5, 300])
+def test_text_lengths_fp32(vds, L):
+    _check_full(vds, (3, 30, 40, 2, 3, 3), 3, 128, L, torch.float32)
+
+
+def test_single_window_is_global_attention(vds):
+    """One window covers the grid: global attention over [video ; text]."""
+    _check_full(vds, (3, 9, 16, 1, 1, 1), 2, 128, 7, torch.bfloat16)
+    _check_full(vds, (3, 9, 16, 1, 1, 1), 2, 64, 7, torch.float32)
+
+
+def test_custom_scale(vds):
+    _check_full(vds, (2, 45, 80, 1, 3, 3), 1, 128, 16, torch.bfloat16, layouts=(op.SHIFTED,), scale=0.05)
+
+
+def test_tiny_windows_and_tail_past_n(vds):
+    """Windows of a few tokens (tiles mostly padding); the last window's tile
+    runs past row N (zero-filled by TMA)."""
+    _check_full(vds, (2, 45, 80, 1, 9, 16), 2, 128, 3, torch.bfloat16)   # 50-token windows, 8 shifted
+    _check_full(vds, (2, 3, 200, 1, 1, 9), 1, 64, 0, torch.bfloat16)
+
+
+def _sampled_check(vds, grid, heads, hd, L, windows_per_layout=4, heads_checked=(0,)):
+    """Full-size run; the oracle computes a few (window, head) pairs, the
+    text partials of those windows, and the text mean for one head over all
+    windows; every video row of the output must be written (no NaN left)."""
+    from video_dit_shifted_gb300 import synth
+    plan = vds.Plan(*grid, device="cuda")
+    N = plan.N
+    x = synth.attention_inputs(N, L, heads, hd, torch.bfloat16, "cuda")
+    rng = np.random.default_rng(1)
+    for layout in (op.REGULAR, op.SHIFTED):
+        o_vid, o_txt, ws = _run(vds, plan, layout, x, heads, hd, L, torch.bfloat16)
+        assert not torch.isnan(o_vid).any()
+        off, ids = op.layout_tables(*grid, layout)
+        nwin = len(off) - 1
+        sizes = np.diff(off)
+        wins = sorted({0, nwin - 1, int(sizes.argmin()), int(sizes.argmax())} |
+                      set(rng.choice(nwin, size=windows_per_layout, replace=False).tolist()))
+        rows = np.concatenate([np.arange(off[w], off[w + 1]) for w in wins])
+        sub = lambda t: _np(t[torch.from_numpy(rows).cuda()])
+        sub_off = np.concatenate([[0], np.cumsum(sizes[wins])])
+        sub_ids = np.arange(rows.size)
+        txt = [_np(x[n]) for n in ("qt", "kt", "vt")]
+        ref_o, ref_t = oa.window_attention(sub(x["q"]), sub(x["k"]), sub(x["v"]), *txt, sub_off, sub_ids,
+                                           heads=heads_checked)
+        got = _np(o_vid[torch.from_numpy(ids[rows]).cuda()])
+        for h in heads_checked:
+            assert np.abs(got[:, h] - ref_o[:, h]).max() <= 2e-2, (layout, h)
+        part = ws[256:].view(torch.float32).view(nwin, L, heads, hd)
+        for i, w in enumerate(wins):
+            for h in heads_checked:
+                assert np.abs(_np(part[w, :, h]) - ref_t[i, :, h]).max() <= 2e-2, (layout, w, h)
+        # o_txt is the ordered mean of the partials, rounded once to bf16
+        mean = part.double().mean(dim=0)
+        assert (o_txt.double() - mean).abs().max().item() <= 4e-3
+    plan.close()
+
+
+def test_720p_sampled(vds):
+    _sampled_check(vds, (21, 45, 80, 4, 3, 3), 24, 128, 256, heads_checked=(0, 23))
+
+
+def test_1080p_sampled(vds):
+    _sampled_check(vds, (21, 68, 120, 4, 3, 3), 24, 128, 256, heads_checked=(5,))
+
+
+def test_bad_alignment_rejected(vds):
+    plan = vds.Plan(2, 45, 80, 1, 3, 3, device="cuda")
+    from video_dit_shifted_gb300 import synth
+    x = synth.attention_inputs(plan.N, 16, 2, 96, torch.bfloat16, "cuda")
+    o = torch.empty((plan.N, 2, 96), dtype=torch.bfloat16, device="cuda")
+    t = torch.empty((16, 2, 96), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    with pytest.raises(vds.wp.WpError) as e:
+        vds.window_attn(plan, op.REGULAR, x["q"], x["k"], x["v"], x["qt"], x["kt"], x["vt"], o, t, ws)
+    assert e.value.code == 2
+    plan.close()

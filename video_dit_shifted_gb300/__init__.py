@@ -1,0 +1,11 @@
+"""Shifted-window video attention for GB300 (sm_103a).
+
+The hot path of NaDiT/SeedVR2-style video DiTs ("Window-Aligned Sequence
+Parallelism (SeedVR2)"): a host window planner, the regular <-> shifted row
+re-layout, and window attention over [video window ; replicated text] with
+the per-window text outputs averaged over the window count.  The compute
+runs in libwp.so (include/wp.h); ``wp`` is its ctypes binding.
+"""
+from . import wp  # noqa: F401
+from .wp import (BF16, CANONICAL, FP32, REGULAR, SHIFTED, Plan, make_workspace,  # noqa: F401
+                 permute, read_status, window_attn, workspace_bytes)

@@ -1,0 +1,288 @@
+// wp_window_attn: argument checks, the fp32 parity kernel and the text mean.
+//
+// "Window-Aligned Sequence Parallelism (SeedVR2)":
+//   §SeedVR2 integration -- one bidirectional attention per
+//     [video window ; replicated text] segment, video rows back to canonical
+//     order;
+//   §Text stream -- text output = (sum over windows of T_w) / window count.
+//
+// The bf16 tensor-core kernel lives in attn_tc.cu.  This file holds
+//   * attn_f32_kernel: fp32 SIMT attention (parity mode, head_dim 64/128),
+//   * text_mean_kernel: o_txt = (sum_w T_w) / nwin, summed in window order by
+//     one thread per output element (no atomics, so the result is
+//     deterministic), and
+//   * the C entry points wp_attn_workspace_bytes / wp_window_attn /
+//     wp_read_status.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+
+#include "attn_internal.h"
+
+namespace wp {
+namespace {
+
+// ------------------------------------------------------------ fp32 path --
+// One block = 32 query rows of one segment (window w, head h); 4 threads per
+// row, each holding every 4th element of the row's head_dim.  Keys stream
+// through shared memory 32 at a time; the softmax is the usual online
+// (running max / running sum) form in fp32 with expf.
+constexpr int kF32Rows = 32;
+constexpr int kF32Keys = 32;
+constexpr int kF32Tpr = 4;
+
+struct F32Params {
+  const float *q, *k, *v, *qt, *kt, *vt;
+  int64_t vid_stride, txt_stride, o_stride;  // in floats
+  float* o_vid;
+  float* partial;
+  const int32_t *win_off, *ids;
+  int heads, L, qblocks;
+  float scale;
+};
+
+template <int HD>
+__global__ void __launch_bounds__(kF32Rows * kF32Tpr) attn_f32_kernel(F32Params p) {
+  constexpr int DPT = HD / kF32Tpr;
+  __shared__ float Ks[kF32Keys][HD];
+  __shared__ float Vs[kF32Keys][HD];
+  const int w = blockIdx.x / p.qblocks;
+  const int qb = blockIdx.x % p.qblocks;
+  const int h = blockIdx.y;
+  const int a = p.win_off[w];
+  const int n_w = p.win_off[w + 1] - a;
+  const int seg = n_w + p.L;
+  if (qb * kF32Rows >= seg) return;  // uniform per block
+  const int row = threadIdx.x / kF32Tpr, part = threadIdx.x % kF32Tpr;
+  const int r = qb * kF32Rows + row;
+  const bool live = r < seg;
+
+  auto qrow = [&](int i) -> const float* {  // segment row i of q
+    return i < n_w ? p.q + (a + i) * p.vid_stride + h * HD : p.qt + (i - n_w) * p.txt_stride + h * HD;
+  };
+  float qr[DPT], acc[DPT];
+#pragma unroll
+  for (int i = 0; i < DPT; ++i) {
+    qr[i] = live ? qrow(r)[i * kF32Tpr + part] : 0.f;
+    acc[i] = 0.f;
+  }
+  float m = -INFINITY, l = 0.f;
+  for (int k0 = 0; k0 < seg; k0 += kF32Keys) {
+    __syncthreads();
+    for (int e = threadIdx.x; e < kF32Keys * HD; e += blockDim.x) {
+      const int j = e / HD, d = e % HD, kk = k0 + j;
+      float kv = 0.f, vv = 0.f;
+      if (kk < n_w) {
+        kv = p.k[(a + kk) * p.vid_stride + h * HD + d];
+        vv = p.v[(a + kk) * p.vid_stride + h * HD + d];
+      } else if (kk < seg) {
+        kv = p.kt[(kk - n_w) * p.txt_stride + h * HD + d];
+        vv = p.vt[(kk - n_w) * p.txt_stride + h * HD + d];
+      }
+      Ks[j][d] = kv;
+      Vs[j][d] = vv;
+    }
+    __syncthreads();
+    const int nk = min(kF32Keys, seg - k0);
+    float s[kF32Keys];
+    float tmax = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kF32Keys; ++j) {
+      float dot = 0.f;
+#pragma unroll
+      for (int i = 0; i < DPT; ++i) dot = fmaf(qr[i], Ks[j][i * kF32Tpr + part], dot);
+      dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+      dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+      s[j] = j < nk ? dot * p.scale : -INFINITY;
+      tmax = fmaxf(tmax, s[j]);
+    }
+    const float m_new = fmaxf(m, tmax);
+    const float alpha = expf(m - m_new);  // m = -inf on the first tile -> 0
+    l *= alpha;
+#pragma unroll
+    for (int i = 0; i < DPT; ++i) acc[i] *= alpha;
+#pragma unroll
+    for (int j = 0; j < kF32Keys; ++j) {
+      const float pj = j < nk ? expf(s[j] - m_new) : 0.f;
+      l += pj;
+#pragma unroll
+      for (int i = 0; i < DPT; ++i) acc[i] = fmaf(pj, Vs[j][i * kF32Tpr + part], acc[i]);
+    }
+    m = m_new;
+  }
+  if (!live) return;
+  const float inv = 1.f / l;
+  float* out = r < n_w ? p.o_vid + static_cast<int64_t>(p.ids[a + r]) * p.o_stride + h * HD
+                       : p.partial + ((static_cast<int64_t>(w) * p.L + (r - n_w)) * p.heads + h) * HD;
+#pragma unroll
+  for (int i = 0; i < DPT; ++i) out[i * kF32Tpr + part] = acc[i] * inv;
+}
+
+// ---------------------------------------------------------- text mean ----
+template <typename OutT>
+__global__ void text_mean_kernel(const float* __restrict__ part, int nwin, int64_t n,
+                                 OutT* __restrict__ out) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const float count = static_cast<float>(nwin);
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+    float acc = 0.f;
+    for (int w = 0; w < nwin; ++w) acc += __ldcs(part + static_cast<int64_t>(w) * n + i);
+    const float mean = acc / count;
+    if constexpr (sizeof(OutT) == 2) {
+      out[i] = __float2bfloat16_rn(mean);
+    } else {
+      out[i] = mean;
+    }
+  }
+}
+
+int launch_text_mean(const AttnCall& c) {
+  const int64_t n = static_cast<int64_t>(c.L) * c.heads * c.hd;
+  if (n == 0) return WP_OK;
+  const int threads = 256;
+  const int64_t blocks = std::min<int64_t>((n + threads - 1) / threads, 152 * 16);
+  if (c.dtype == WP_BF16)
+    text_mean_kernel<__nv_bfloat16><<<static_cast<unsigned>(blocks), threads, 0, c.stream>>>(
+        c.partial, c.nwin, n, static_cast<__nv_bfloat16*>(c.o_txt));
+  else
+    text_mean_kernel<float><<<static_cast<unsigned>(blocks), threads, 0, c.stream>>>(
+        c.partial, c.nwin, n, static_cast<float*>(c.o_txt));
+  return cuda_check(cudaGetLastError(), "text_mean_kernel launch");
+}
+
+}  // namespace
+
+int launch_attn_f32(const AttnCall& c) {
+  F32Params p;
+  p.q = static_cast<const float*>(c.q);
+  p.k = static_cast<const float*>(c.k);
+  p.v = static_cast<const float*>(c.v);
+  p.qt = static_cast<const float*>(c.qt);
+  p.kt = static_cast<const float*>(c.kt);
+  p.vt = static_cast<const float*>(c.vt);
+  p.vid_stride = c.vid_stride_B / 4;
+  p.txt_stride = c.txt_stride_B / 4;
+  p.o_stride = c.o_stride_B / 4;
+  p.o_vid = static_cast<float*>(c.o_vid);
+  p.partial = c.partial;
+  p.win_off = c.win_off;
+  p.ids = c.ids;
+  p.heads = c.heads;
+  p.L = c.L;
+  p.qblocks = (c.max_tokens + c.L + kF32Rows - 1) / kF32Rows;
+  p.scale = c.scale;
+  const int64_t gx = static_cast<int64_t>(c.nwin) * p.qblocks;
+  if (gx > 0x7fffffff) return fail(WP_EUNSUPPORTED, "fp32 grid too large");
+  dim3 grid(static_cast<unsigned>(gx), c.heads);
+  if (c.hd == 64)
+    attn_f32_kernel<64><<<grid, kF32Rows * kF32Tpr, 0, c.stream>>>(p);
+  else
+    attn_f32_kernel<128><<<grid, kF32Rows * kF32Tpr, 0, c.stream>>>(p);
+  return cuda_check(cudaGetLastError(), "attn_f32_kernel launch");
+}
+
+}  // namespace wp
+
+using namespace wp;
+
+namespace {
+
+int workspace_bytes(const wp_plan* plan, int layout, int heads, int hd, int L, size_t* bytes) {
+  const int64_t part = static_cast<int64_t>(plan->lay[layout].nwin) * L * heads * hd * 4;
+  *bytes = kStatusBytes + static_cast<size_t>(part);
+  return WP_OK;
+}
+
+int check_shape(const wp_plan* plan, int layout, int heads, int hd, int L, int dtype) {
+  if (!plan) return fail(WP_EINVAL, "plan is NULL");
+  if (layout != WP_REGULAR && layout != WP_SHIFTED)
+    return fail(WP_EINVAL, "attention layout must be WP_REGULAR or WP_SHIFTED (got %d)", layout);
+  if (heads < 1 || heads > 65535) return fail(WP_EINVAL, "heads=%d out of range [1, 65535]", heads);
+  if (L < 0) return fail(WP_EINVAL, "L=%d < 0", L);
+  if (dtype != WP_BF16 && dtype != WP_FP32) return fail(WP_EINVAL, "bad dtype %d", dtype);
+  if (hd != 64 && hd != 128) return fail(WP_EUNSUPPORTED, "head_dim=%d (supported: 64, 128)", hd);
+  return WP_OK;
+}
+
+}  // namespace
+
+extern "C" int wp_attn_workspace_bytes(const wp_plan* plan, int layout, int heads, int head_dim,
+                                       int L, int dtype, size_t* bytes) {
+  if (int rc = check_shape(plan, layout, heads, head_dim, L, dtype)) return rc;
+  if (!bytes) return fail(WP_EINVAL, "bytes is NULL");
+  workspace_bytes(plan, layout, heads, head_dim, L, bytes);
+  return ok();
+}
+
+extern "C" int wp_window_attn(const wp_plan* plan, int layout, int heads, int head_dim, int L,
+                              int dtype, const void* q, const void* k, const void* v,
+                              int64_t vid_row_stride_B, const void* qt, const void* kt,
+                              const void* vt, int64_t txt_row_stride_B, void* o_vid,
+                              int64_t o_vid_row_stride_B, void* o_txt, void* workspace,
+                              size_t ws_bytes, float softmax_scale, void* stream) {
+  if (int rc = check_shape(plan, layout, heads, head_dim, L, dtype)) return rc;
+  if (!q || !k || !v || !o_vid || !workspace) return fail(WP_EINVAL, "q, k, v, o_vid or workspace is NULL");
+  if (L > 0 && (!qt || !kt || !vt || !o_txt)) return fail(WP_EINVAL, "text pointers are NULL with L=%d", L);
+  const int64_t elem = dtype == WP_BF16 ? 2 : 4;
+  const int64_t row_B = static_cast<int64_t>(heads) * head_dim * elem;
+  for (const void* ptr : {q, k, v, static_cast<const void*>(o_vid), static_cast<const void*>(workspace)})
+    if (!aligned16(ptr)) return fail(WP_EUNSUPPORTED, "q/k/v/o_vid/workspace must be 16-byte aligned");
+  if (L > 0)
+    for (const void* ptr : {qt, kt, vt, static_cast<const void*>(o_txt)})
+      if (!aligned16(ptr)) return fail(WP_EUNSUPPORTED, "qt/kt/vt/o_txt must be 16-byte aligned");
+  auto stride_ok = [&](int64_t s) { return s >= row_B && (s & 15) == 0; };
+  if (!stride_ok(vid_row_stride_B) || !stride_ok(o_vid_row_stride_B) || (L > 0 && !stride_ok(txt_row_stride_B)))
+    return fail(WP_EUNSUPPORTED,
+                "row strides (video %lld, text %lld, out %lld) must be multiples of 16 and >= %lld",
+                (long long)vid_row_stride_B, (long long)txt_row_stride_B, (long long)o_vid_row_stride_B,
+                (long long)row_B);
+  size_t need = 0;
+  workspace_bytes(plan, layout, heads, head_dim, L, &need);
+  if (ws_bytes < need) return fail(WP_EINVAL, "workspace too small: %zu < %zu bytes", ws_bytes, need);
+  if (int rc = require_uploaded(plan)) return rc;
+
+  const LayoutTables& LT = plan->lay[layout];
+  AttnCall c{};
+  c.layout = layout; c.heads = heads; c.hd = head_dim; c.L = L; c.dtype = dtype;
+  c.q = q; c.k = k; c.v = v; c.vid_stride_B = vid_row_stride_B;
+  c.qt = qt; c.kt = kt; c.vt = vt; c.txt_stride_B = txt_row_stride_B;
+  c.o_vid = o_vid; c.o_stride_B = o_vid_row_stride_B; c.o_txt = o_txt;
+  c.status = static_cast<int*>(workspace);
+  c.partial = reinterpret_cast<float*>(static_cast<char*>(workspace) + kStatusBytes);
+  c.scale = softmax_scale > 0.f ? softmax_scale : 1.f / std::sqrt(static_cast<float>(head_dim));
+  c.stream = static_cast<cudaStream_t>(stream);
+  c.N = plan->N;
+  c.nwin = LT.nwin;
+  c.max_tokens = LT.max_tokens;
+  c.win_off = dev_ptr<int32_t>(plan, plan->dlay[layout].win_off);
+  c.ids = dev_ptr<int32_t>(plan, plan->dlay[layout].ids);
+  c.pair_off[0] = dev_ptr<int32_t>(plan, plan->dlay[layout].pair_off[0]);
+  c.pair_off[1] = dev_ptr<int32_t>(plan, plan->dlay[layout].pair_off[1]);
+  c.text_tiles = (L + kTileM - 1) / kTileM;
+  const int64_t pairs = static_cast<int64_t>(LT.pair_off[c.text_tiles & 1][LT.nwin]) +
+                        static_cast<int64_t>(LT.nwin) * (c.text_tiles >> 1);
+  if (pairs > 0x7fffffff) return fail(WP_EUNSUPPORTED, "too many query tiles");
+  c.total_pairs = static_cast<int>(pairs);
+
+  if (int rc = cuda_check(cudaMemsetAsync(workspace, 0, kStatusBytes, c.stream), "cudaMemsetAsync(status)"))
+    return rc;
+  int rc = dtype == WP_BF16 ? launch_attn_bf16_tc(c) : launch_attn_f32(c);
+  if (rc) return rc;
+  if (L > 0)
+    if ((rc = launch_text_mean(c))) return rc;
+  return ok();
+}
+
+extern "C" int wp_read_status(const void* workspace, int* device_status, void* stream) {
+  if (!workspace || !device_status) return fail(WP_EINVAL, "workspace or device_status is NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int host = 0;
+  if (int rc = cuda_check(cudaMemcpyAsync(&host, workspace, sizeof(int), cudaMemcpyDeviceToHost, s),
+                          "cudaMemcpyAsync(status)"))
+    return rc;
+  if (int rc = cuda_check(cudaStreamSynchronize(s), "cudaStreamSynchronize(status)")) return rc;
+  *device_status = host;
+  return ok();
+}

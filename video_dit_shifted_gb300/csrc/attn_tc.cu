@@ -1,0 +1,613 @@
+// Window attention on the sm_103a tensor cores (tcgen05 + TMEM + TMA), bf16
+// in, fp32 accumulation.
+//
+// What it computes ("Window-Aligned Sequence Parallelism (SeedVR2)",
+// §SeedVR2 integration and §Text stream): for every window w and head h, one
+// full attention over the segment [video rows of w ; text rows]; video
+// results are scattered to their canonical rows, text results T_w are written
+// in fp32 for the ordered mean in attn.cu.
+//
+// Design (one CTA per pair of 128-row query tiles of one (window, head)):
+//   warp 0      TMA producer: Q tiles once, then K and V tiles of the segment
+//               (video tiles of the window, then text tiles) into a 2-stage
+//               ring each, 128-byte swizzled, 64 columns per box;
+//   warp 1      MMA issuer (one thread): S_i = Q_i K_j^T (SS form) into TMEM,
+//               O_i += P_i V_j with P_i read from TMEM (TS form);
+//   warp 2      TMEM allocator (512 columns: S0, S1, O0, O1);
+//   warps 4-7   softmax for query tile 0, warps 8-11 for query tile 1: one
+//               thread per query row (TMEM lane), online softmax in the log2
+//               domain, P written back over S as packed bf16, O rescaled in
+//               TMEM only when the running max grows by more than 2^8 (the
+//               final O / l is exact either way), then the epilogue.
+// The two query tiles share every K/V tile, and the MMA order
+// S0(j) S1(j) PV0(j) S0(j+1) PV1(j) S1(j+1) ... lets one tile's softmax run
+// while the tensor core works on the other.
+//
+// Masking: a segment is ragged, so the last video K/V tile of a window may
+// run into the next window's rows (or past N, where TMA fills zeros).  Those
+// key columns get probability exactly 0 and are left out of the max.  Query
+// rows past the window are computed but never stored.
+//
+// Every mbarrier wait is bounded (kWaitTimeoutNs); on expiry the kernel sets
+// WP_ETIMEOUT in the status word, raises a CTA-wide abort flag, drains its
+// own TMA and MMA work and frees TMEM before returning.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstring>
+
+#include "attn_internal.h"
+
+namespace wp {
+namespace {
+
+constexpr int kBM = 128;  // query rows per tile (TMEM lanes)
+constexpr int kBN = 128;  // keys per K/V tile
+constexpr int kThreads = 384;
+constexpr int kTmemCols = 512;
+static_assert(kBM == kTileM, "plan tables count tiles of kTileM rows");
+
+template <int HD>
+struct Cfg {
+  static constexpr int kHalves = HD / 64;          // 64-column (128 B) swizzle blocks
+  static constexpr int kBoxBytes = 128 * 128;      // one 128-row x 128-byte box
+  static constexpr int kTileBytes = kBM * HD * 2;  // a Q, K or V tile
+  static constexpr int kQ = 0;                     // Q tile i at kQ + i*kTileBytes
+  static constexpr int kK = 2 * kTileBytes;        // K stage s at kK + s*kTileBytes
+  static constexpr int kV = 4 * kTileBytes;        // V stage s at kV + s*kTileBytes
+  static constexpr int kBar = 6 * kTileBytes;
+  static constexpr int kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + HD;
+};
+// Both head dims request the HD=128 footprint so that exactly one CTA (and
+// one 512-column TMEM allocation) lives on an SM.
+constexpr int kSmemBytes = Cfg<128>::kBar + 256 + 1024;
+
+struct Barriers {
+  uint64_t q_full;
+  uint64_t k_full[2], v_full[2], k_empty[2], v_empty[2];
+  uint64_t s_full[2], p_full[2], o_full[2];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+static_assert(sizeof(Barriers) <= 256, "barrier block");
+
+struct TcParams {
+  const int32_t* win_off;
+  const int32_t* ids;
+  const int32_t* pair_off;  // pair_off[text_tiles & 1]
+  int pair_add;             // text_tiles >> 1
+  int nwin, L, heads, text_tiles;
+  __nv_bfloat16* o_vid;
+  int64_t o_stride;  // elements
+  float* partial;
+  int* status;
+  float scale_log2;
+};
+
+// ------------------------------------------------------------ PTX helpers --
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Bounded wait for the phase with the given parity.  Returns false if the
+// CTA is aborting (flag set by any thread) or this wait expired (then it
+// sets the flag and the status word).
+__device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                        int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 63) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > kWaitTimeoutNs) {
+        *abort_flag = 1;
+        atomicCAS(status, 0, WP_ETIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// Bounded wait that ignores the abort flag (used while draining).
+__device__ __noinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer() - t0 > kWaitTimeoutNs) return;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x,
+                                            int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (layout code 2 in bits
+// 61-63), descriptor version 1 (bits 46-47), base offset 0 (every swizzle
+// atom is 1024-byte aligned).  lbo/sbo in bytes.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((saddr & 0x3FFFF) >> 4) |
+         (static_cast<uint64_t>((lbo >> 4) & 0x3FFF) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFF) << 32) | (uint64_t(1) << 46) |
+         (uint64_t(2) << 61);
+}
+
+// Instruction descriptor for kind::f16: D fp32 (bits 4-5 = 1), A and B bf16
+// (bits 7-9, 10-12 = 1), B transposed (MN-major) via bit 16, N>>3 in bits
+// 17-22, M>>4 in bits 24-28.
+constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                       uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+// 32 lanes x 32 columns of 32-bit from TMEM, waited on before returning.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
+      "%30, %31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, "
+      "%29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+      "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]),
+      "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]),
+      "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  uint32_t u;
+  memcpy(&u, &v, 4);
+  return u;
+}
+
+// ------------------------------------------------------------------ kernel --
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_qt,
+                   const __grid_constant__ CUtensorMap tm_kt, const __grid_constant__ CUtensorMap tm_vt,
+                   const TcParams p) {
+  using C = Cfg<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;  // 1024-aligned for 128 B swizzle
+  uint8_t* smem = smem_raw + (base - raw);
+  Barriers* bars = reinterpret_cast<Barriers*>(smem + C::kBar);
+  volatile int* abort_flag = &bars->abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.y;
+
+  // ---- work item: which window, which pair of query tiles --------------
+  const int pidx = blockIdx.x;
+  int lo = 0, hi = p.nwin - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(p.pair_off + mid) + mid * p.pair_add <= pidx) lo = mid; else hi = mid - 1;
+  }
+  const int w = lo;
+  const int a = __ldg(p.win_off + w);
+  const int n_w = __ldg(p.win_off + w + 1) - a;
+  const int vt = (n_w + kBN - 1) / kBN;  // video tiles (queries and keys alike)
+  const int tt = p.text_tiles;
+  const int nkv = vt + tt;
+  const int t0 = 2 * (pidx - (__ldg(p.pair_off + w) + w * p.pair_add));
+  const int nq = min(2, nkv - t0);
+
+  const uint32_t bq_full = smem_addr(&bars->q_full);
+  auto bar = [](uint64_t& b) { return smem_addr(&b); };
+
+  if (threadIdx.x == 0) {
+    mbar_init(bq_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(bars->k_full[s]), 1);
+      mbar_init(bar(bars->v_full[s]), 1);
+      mbar_init(bar(bars->k_empty[s]), 1);
+      mbar_init(bar(bars->v_empty[s]), 1);
+      mbar_init(bar(bars->s_full[s]), 1);
+      mbar_init(bar(bars->p_full[s]), 128);
+      mbar_init(bar(bars->o_full[s]), 1);
+    }
+    mbar_init(bar(bars->mma_done), 1);
+    // A CTA of this launch already failed: skip the work so that a broken
+    // launch ends quickly instead of timing out CTA after CTA.
+    bars->abort_flag = *reinterpret_cast<volatile int*>(p.status) != 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (bars->abort_flag) return;
+  if (warp == 2) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(&bars->tmem_base)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 0) {
+    // ======================= TMA producer ===============================
+    if (lane == 0) {
+      int issued_k = 0, issued_v = 0;
+      bool good = true;
+      mbar_expect_tx(bq_full, nq * C::kTileBytes);
+      for (int i = 0; i < nq; ++i) {
+        const int t = t0 + i;
+        const CUtensorMap* map = t < vt ? &tm_q : &tm_qt;
+        const int row = t < vt ? a + t * kBM : (t - vt) * kBM;
+        for (int hf = 0; hf < C::kHalves; ++hf)
+          tma_load_2d(base + C::kQ + i * C::kTileBytes + hf * C::kBoxBytes, map, bq_full,
+                      h * HD + hf * 64, row);
+      }
+      for (int j = 0; j < nkv && good; ++j) {
+        const int s = j & 1;
+        const bool vid = j < vt;
+        const int row = vid ? a + j * kBN : (j - vt) * kBN;
+        if (j >= 2 && !(good = wait_phase(bar(bars->k_empty[s]), ((j >> 1) - 1) & 1, abort_flag, p.status)))
+          break;
+        mbar_expect_tx(bar(bars->k_full[s]), C::kTileBytes);
+        for (int hf = 0; hf < C::kHalves; ++hf)
+          tma_load_2d(base + C::kK + s * C::kTileBytes + hf * C::kBoxBytes, vid ? &tm_k : &tm_kt,
+                      bar(bars->k_full[s]), h * HD + hf * 64, row);
+        ++issued_k;
+        if (j >= 2 && !(good = wait_phase(bar(bars->v_empty[s]), ((j >> 1) - 1) & 1, abort_flag, p.status)))
+          break;
+        mbar_expect_tx(bar(bars->v_full[s]), C::kTileBytes);
+        for (int hf = 0; hf < C::kHalves; ++hf)
+          tma_load_2d(base + C::kV + s * C::kTileBytes + hf * C::kBoxBytes, vid ? &tm_v : &tm_vt,
+                      bar(bars->v_full[s]), h * HD + hf * 64, row);
+        ++issued_v;
+      }
+      if (*abort_flag) {
+        // Let every copy this thread started land before the CTA exits.
+        drain_wait(bq_full, 0);
+        for (int u = issued_k - 2; u < issued_k; ++u)
+          if (u >= 0) drain_wait(bar(bars->k_full[u & 1]), (u >> 1) & 1);
+        for (int u = issued_v - 2; u < issued_v; ++u)
+          if (u >= 0) drain_wait(bar(bars->v_full[u & 1]), (u >> 1) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ======================= MMA issuer =================================
+    if (lane == 0) {
+      constexpr uint32_t kIdescQK = idesc_bf16(kBM, kBN, false);
+      constexpr uint32_t kIdescPV = idesc_bf16(kBM, HD, true);
+      const uint32_t colS[2] = {tmem + C::kColS0, tmem + C::kColS1};
+      const uint32_t colO[2] = {tmem + C::kColO0, tmem + C::kColO1};
+      auto issue_qk = [&](int i, int s) {
+        const uint32_t qa = base + C::kQ + i * C::kTileBytes;
+        const uint32_t kb = base + C::kK + s * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
+          mma_ss(colS[i], sw128_desc(qa + off, 16, 1024), sw128_desc(kb + off, 16, 1024), kIdescQK,
+                 kk > 0);
+        }
+      };
+      auto issue_pv = [&](int i, int s, bool first) {
+        const uint32_t vb = base + C::kV + s * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_ts(colO[i], colS[i] + kk * 8, sw128_desc(vb + kk * 2048, C::kBoxBytes, 1024), kIdescPV,
+                 (!first || kk > 0) ? 1u : 0u);
+      };
+      bool good = wait_phase(bq_full, 0, abort_flag, p.status) &&
+                  wait_phase(bar(bars->k_full[0]), 0, abort_flag, p.status);
+      if (good) {
+        tc_fence_after();
+        for (int i = 0; i < nq; ++i) {
+          issue_qk(i, 0);
+          mma_commit(bar(bars->s_full[i]));
+        }
+        mma_commit(bar(bars->k_empty[0]));
+      }
+      for (int j = 0; j < nkv && good; ++j) {
+        const int s = j & 1, sn = (j + 1) & 1;
+        const bool more = j + 1 < nkv;
+        if (!(good = wait_phase(bar(bars->v_full[s]), (j >> 1) & 1, abort_flag, p.status))) break;
+        for (int i = 0; i < nq; ++i) {
+          if (!(good = wait_phase(bar(bars->p_full[i]), j & 1, abort_flag, p.status))) break;
+          tc_fence_after();
+          issue_pv(i, s, j == 0);
+          if (!more) mma_commit(bar(bars->o_full[i]));
+          if (more) {
+            if (i == 0 && !(good = wait_phase(bar(bars->k_full[sn]), ((j + 1) >> 1) & 1, abort_flag, p.status)))
+              break;
+            tc_fence_after();
+            issue_qk(i, sn);
+            mma_commit(bar(bars->s_full[i]));
+          }
+        }
+        if (!good) break;
+        mma_commit(bar(bars->v_empty[s]));
+        if (more) mma_commit(bar(bars->k_empty[sn]));
+      }
+      // All MMAs this thread issued must finish before TMEM is freed.
+      mma_commit(bar(bars->mma_done));
+      drain_wait(bar(bars->mma_done), 0);
+    }
+  } else if (warp >= 4) {
+    // ======================= softmax + epilogue =========================
+    const int i = (warp - 4) >> 2;  // query tile of this warpgroup
+    const int quarter = warp & 3;   // TMEM lanes 32*quarter .. +31
+    const int r = quarter * 32 + lane;
+    if (i < nq) {
+      const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+      const uint32_t tS = tmem + (i == 0 ? C::kColS0 : C::kColS1) + lane_off;
+      const uint32_t tO = tmem + (i == 0 ? C::kColO0 : C::kColO1) + lane_off;
+      const uint32_t bs = bar(bars->s_full[i]), bp = bar(bars->p_full[i]);
+      float m_run = 0.f, l_run = 0.f;
+      bool good = true;
+      for (int j = 0; j < nkv; ++j) {
+        const int valid = j < vt ? min(kBN, n_w - j * kBN) : min(kBN, p.L - (j - vt) * kBN);
+        good = __all_sync(0xffffffffu, wait_phase(bs, j & 1, abort_flag, p.status));
+        if (!good) break;
+        tc_fence_after();
+        uint32_t s[32];
+        float mx = -INFINITY;
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+          tmem_ld32(tS + c * 32, s);
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (c * 32 + e < valid) mx = fmaxf(mx, __uint_as_float(s[e]));
+        }
+        mx *= p.scale_log2;
+        if (j == 0) {
+          m_run = mx;
+        } else if (__any_sync(0xffffffffu, mx > m_run + 8.f)) {
+          const float m_new = fmaxf(m_run, mx);
+          const float alpha = ex2(m_run - m_new);
+          l_run *= alpha;
+          m_run = m_new;
+#pragma unroll 1
+          for (int c = 0; c < HD / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + c * 32, o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(tO + c * 32, o);
+          }
+        }
+        float sum = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+          tmem_ld32(tS + c * 32, s);
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float p0 = (c * 32 + e < valid) ? ex2(fmaf(__uint_as_float(s[e]), p.scale_log2, -m_run)) : 0.f;
+            const float p1 =
+                (c * 32 + e + 1 < valid) ? ex2(fmaf(__uint_as_float(s[e + 1]), p.scale_log2, -m_run)) : 0.f;
+            sum += p0 + p1;
+            pk[e >> 1] = pack_bf16(p0, p1);
+          }
+          // P (bf16, 2 per column) overwrites S columns already consumed.
+          tmem_st16(tS + c * 16, pk);
+        }
+        l_run += sum;
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bp);
+      }
+      if (good) good = __all_sync(0xffffffffu, wait_phase(bar(bars->o_full[i]), 0, abort_flag, p.status));
+      if (good) {
+        tc_fence_after();
+        const int t = t0 + i;
+        const float inv_l = 1.f / l_run;
+        if (t < vt) {
+          const int tok = t * kBM + r;
+          const bool live = tok < n_w;
+          __nv_bfloat16* dst =
+              live ? p.o_vid + static_cast<int64_t>(__ldg(p.ids + a + tok)) * p.o_stride + h * HD : nullptr;
+#pragma unroll 1
+          for (int c = 0; c < HD / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + c * 32, o);
+            if (live) {
+              uint32_t pk[16];
+#pragma unroll
+              for (int e = 0; e < 32; e += 2)
+                pk[e >> 1] = pack_bf16(__uint_as_float(o[e]) * inv_l, __uint_as_float(o[e + 1]) * inv_l);
+              uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4)
+                d4[q4] = make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+            }
+          }
+        } else {
+          const int lt = (t - vt) * kBM + r;
+          const bool live = lt < p.L;
+          float* dst = live ? p.partial + ((static_cast<int64_t>(w) * p.L + lt) * p.heads + h) * HD : nullptr;
+#pragma unroll 1
+          for (int c = 0; c < HD / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + c * 32, o);
+            if (live) {
+              float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+#pragma unroll
+              for (int q4 = 0; q4 < 8; ++q4)
+                d4[q4] = make_float4(__uint_as_float(o[4 * q4]) * inv_l, __uint_as_float(o[4 * q4 + 1]) * inv_l,
+                                     __uint_as_float(o[4 * q4 + 2]) * inv_l,
+                                     __uint_as_float(o[4 * q4 + 3]) * inv_l);
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+// ------------------------------------------------------------------- host --
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// 2D bf16 map over rows x (heads*hd) columns, box 128 rows x 64 columns,
+// 128-byte swizzle; reads past the last row return zeros.
+int make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int64_t stride_B) {
+  auto fn = encode_fn();
+  if (!fn) return fail(WP_ECUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(stride_B)};
+  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(WP_ECUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
+  return WP_OK;
+}
+
+template <int HD>
+int launch(const AttnCall& c) {
+  CUtensorMap mq, mk, mv, mqt, mkt, mvt;
+  const int64_t cols = static_cast<int64_t>(c.heads) * HD;
+  if (int rc = make_map(&mq, c.q, c.N, cols, c.vid_stride_B)) return rc;
+  if (int rc = make_map(&mk, c.k, c.N, cols, c.vid_stride_B)) return rc;
+  if (int rc = make_map(&mv, c.v, c.N, cols, c.vid_stride_B)) return rc;
+  if (c.L > 0) {
+    if (int rc = make_map(&mqt, c.qt, c.L, cols, c.txt_stride_B)) return rc;
+    if (int rc = make_map(&mkt, c.kt, c.L, cols, c.txt_stride_B)) return rc;
+    if (int rc = make_map(&mvt, c.vt, c.L, cols, c.txt_stride_B)) return rc;
+  } else {
+    mqt = mq; mkt = mk; mvt = mv;  // never read: there are no text tiles
+  }
+  TcParams p;
+  p.win_off = c.win_off;
+  p.ids = c.ids;
+  p.pair_off = c.pair_off[c.text_tiles & 1];
+  p.pair_add = c.text_tiles >> 1;
+  p.nwin = c.nwin;
+  p.L = c.L;
+  p.heads = c.heads;
+  p.text_tiles = c.text_tiles;
+  p.o_vid = static_cast<__nv_bfloat16*>(c.o_vid);
+  p.o_stride = c.o_stride_B / 2;
+  p.partial = c.partial;
+  p.status = c.status;
+  p.scale_log2 = c.scale * 1.4426950408889634f;
+  auto kern = attn_tc_kernel<HD>;
+  if (int rc = cuda_check(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes),
+                          "cudaFuncSetAttribute(attn_tc_kernel)"))
+    return rc;
+  dim3 grid(static_cast<unsigned>(c.total_pairs), static_cast<unsigned>(c.heads));
+  kern<<<grid, kThreads, kSmemBytes, c.stream>>>(mq, mk, mv, mqt, mkt, mvt, p);
+  return cuda_check(cudaGetLastError(), "attn_tc_kernel launch");
+}
+
+}  // namespace
+
+int launch_attn_bf16_tc(const AttnCall& c) { return c.hd == 64 ? launch<64>(c) : launch<128>(c); }
+
+}  // namespace wp

@@ -1,0 +1,200 @@
+"""Thin ctypes binding of libwp (include/wp.h).
+
+Argument marshalling only: every step of the path runs in libwp's CUDA
+kernels.  PyTorch supplies device memory and the current stream.  If the
+library is missing, every call raises -- there is no fallback.
+"""
+import ctypes
+import os
+
+import numpy as np
+import torch
+
+CANONICAL, REGULAR, SHIFTED = 0, 1, 2
+BF16, FP32 = 0, 1
+STATUS_NAMES = {0: "WP_OK", 1: "WP_EINVAL", 2: "WP_EUNSUPPORTED", 3: "WP_ECUDA",
+                4: "WP_ETIMEOUT", 5: "WP_EDEVICE", 6: "WP_ENOTREADY"}
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libwp.so")
+_lib = None
+
+_c_int, _c_i64, _c_sz, _vp = ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p
+_pi32 = ctypes.POINTER(ctypes.c_int32)
+
+# name -> (restype, argtypes); mirrors include/wp.h
+SIGNATURES = {
+    "wp_plan_create": (_c_int, [_c_int] * 6 + [ctypes.POINTER(_vp)]),
+    "wp_plan_destroy": (None, [_vp]),
+    "wp_plan_info": (_c_int, [_vp, _c_int, ctypes.POINTER(_c_i64)] + [ctypes.POINTER(_c_int)] * 5),
+    "wp_plan_host_tables": (_c_int, [_vp, _c_int, _pi32, _pi32, _pi32]),
+    "wp_plan_device_bytes": (_c_int, [_vp, ctypes.POINTER(_c_sz)]),
+    "wp_plan_upload": (_c_int, [_vp, _vp, _c_sz, _vp]),
+    "wp_permute": (_c_int, [_vp, _c_int, _c_int, _vp, _c_i64, _vp, _c_i64, _c_i64, _vp]),
+    "wp_attn_workspace_bytes": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                         ctypes.POINTER(_c_sz)]),
+    "wp_window_attn": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                _vp, _vp, _vp, _c_i64, _vp, _vp, _vp, _c_i64,
+                                _vp, _c_i64, _vp, _vp, _c_sz, ctypes.c_float, _vp]),
+    "wp_read_status": (_c_int, [_vp, ctypes.POINTER(_c_int), _vp]),
+    "wp_last_error": (ctypes.c_char_p, []),
+    "wp_abi_version": (_c_int, []),
+}
+
+
+class WpError(RuntimeError):
+    def __init__(self, fn, code, msg):
+        super().__init__("%s -> %s: %s" % (fn, STATUS_NAMES.get(code, code), msg))
+        self.code = code
+
+
+def lib():
+    """The loaded libwp (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError("libwp.so is not built (run __graft_entry__.build()); "
+                               "there is no fallback path")
+        l = ctypes.CDLL(_LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(l, name)
+            f.restype, f.argtypes = res, args
+        _lib = l
+    return _lib
+
+
+def _check(fn, code):
+    if code != 0:
+        raise WpError(fn, code, lib().wp_last_error().decode())
+
+
+def _stream_ptr(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+class Plan:
+    """Window geometry of one (T, H, W) grid; optionally uploaded to a GPU."""
+
+    def __init__(self, T, H, W, nt, nh, nw, device=None, stream=None):
+        h = ctypes.c_void_p()
+        _check("wp_plan_create", lib().wp_plan_create(T, H, W, nt, nh, nw, ctypes.byref(h)))
+        self._h = h
+        self.T, self.H, self.W, self.nt, self.nh, self.nw = T, H, W, nt, nh, nw
+        self.N = T * H * W
+        self.dev_buf = None
+        if device is not None:
+            self.upload(device, stream)
+
+    @property
+    def handle(self):
+        if self._h is None:
+            raise RuntimeError("plan is closed")
+        return self._h
+
+    def info(self, layout):
+        n = _c_i64()
+        vals = [_c_int() for _ in range(5)]
+        _check("wp_plan_info", lib().wp_plan_info(self.handle, layout, ctypes.byref(n),
+                                                  *[ctypes.byref(v) for v in vals]))
+        nwin, wt, wh, ww, mx = (v.value for v in vals)
+        return {"n_tokens": n.value, "nwin": nwin, "window": (wt, wh, ww), "max_tokens": mx}
+
+    def host_tables(self, layout):
+        nwin = self.info(layout)["nwin"]
+        off = np.zeros(nwin + 1, np.int32)
+        ids = np.zeros(self.N, np.int32)
+        boxes = np.zeros(nwin * 6, np.int32)
+        p = lambda a: a.ctypes.data_as(_pi32)
+        _check("wp_plan_host_tables", lib().wp_plan_host_tables(self.handle, layout, p(off), p(ids), p(boxes)))
+        return off, ids, boxes.reshape(nwin, 6)
+
+    def device_bytes(self):
+        b = _c_sz()
+        _check("wp_plan_device_bytes", lib().wp_plan_device_bytes(self.handle, ctypes.byref(b)))
+        return b.value
+
+    def upload(self, device, stream=None):
+        device = torch.device(device)
+        nbytes = self.device_bytes()
+        with torch.cuda.device(device):
+            buf = torch.empty(nbytes + 256, dtype=torch.uint8, device=device)
+            off = (-buf.data_ptr()) % 256
+            view = buf[off:off + nbytes]
+            _check("wp_plan_upload", lib().wp_plan_upload(self.handle, _ptr(view), nbytes, _stream_ptr(stream)))
+        self.dev_buf = buf
+        self.device = device
+
+    def close(self):
+        if self._h is not None:
+            lib().wp_plan_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def permute(plan, src, dst, src_layout, dst_layout, stream=None):
+    """dst[q] = src[row of src_layout holding canonical token ids_dst[q]].
+
+    src, dst: 2-D CUDA tensors [N, ...] (rows may be strided; row bytes are
+    the product of the inner dims times the element size)."""
+    row_B = src[0].numel() * src.element_size()
+    _check("wp_permute", lib().wp_permute(plan.handle, src_layout, dst_layout, _ptr(src),
+                                          src.stride(0) * src.element_size(), _ptr(dst),
+                                          dst.stride(0) * dst.element_size(), row_B,
+                                          _stream_ptr(stream)))
+    return dst
+
+
+def _dtype_code(t):
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return FP32
+    raise TypeError("q/k/v must be bfloat16 or float32, got %s" % t.dtype)
+
+
+def workspace_bytes(plan, layout, heads, head_dim, L, dtype_code):
+    b = _c_sz()
+    _check("wp_attn_workspace_bytes", lib().wp_attn_workspace_bytes(
+        plan.handle, layout, heads, head_dim, L, dtype_code, ctypes.byref(b)))
+    return b.value
+
+
+def make_workspace(plan, layout, heads, head_dim, L, dtype_code, device):
+    return torch.empty(workspace_bytes(plan, layout, heads, head_dim, L, dtype_code),
+                       dtype=torch.uint8, device=device)
+
+
+def window_attn(plan, layout, q, k, v, qt, kt, vt, o_vid, o_txt, workspace, scale=0.0, stream=None):
+    """One layer of window attention (see wp_window_attn in include/wp.h).
+
+    q, k, v: [N, heads, hd] views in `layout` order sharing one row stride;
+    qt, kt, vt: [L, heads, hd] sharing one row stride; o_vid [N, heads, hd]
+    (canonical order); o_txt [L, heads, hd] contiguous."""
+    N, heads, hd = q.shape
+    L = qt.shape[0] if qt is not None else 0
+    es = q.element_size()
+    if not (k.stride(0) == v.stride(0) == q.stride(0)):
+        raise ValueError("q, k, v must share one row stride")
+    txt_stride = qt.stride(0) * es if L else 0
+    _check("wp_window_attn", lib().wp_window_attn(
+        plan.handle, layout, heads, hd, L, _dtype_code(q),
+        _ptr(q), _ptr(k), _ptr(v), q.stride(0) * es,
+        _ptr(qt if L else None), _ptr(kt if L else None), _ptr(vt if L else None), txt_stride,
+        _ptr(o_vid), o_vid.stride(0) * es, _ptr(o_txt if L else None),
+        _ptr(workspace), workspace.numel(), float(scale), _stream_ptr(stream)))
+    return o_vid, o_txt
+
+
+def read_status(workspace, stream=None):
+    st = _c_int()
+    _check("wp_read_status", lib().wp_read_status(_ptr(workspace), ctypes.byref(st), _stream_ptr(stream)))
+    return st.value
