@@ -39,13 +39,16 @@
 #include <cstring>
 
 #include "attn_internal.h"
+#include "tmem_io.cuh"
 
 namespace wp {
 namespace {
 
 constexpr int kBM = 128;  // query rows per tile (TMEM lanes)
 constexpr int kBN = 128;  // keys per K/V tile
-constexpr int kThreads = 384;
+constexpr int kThreads = 320;       // warps 0-7 softmax, 8 TMA, 9 MMA
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
 constexpr int kTmemCols = 512;
 static_assert(kBM == kTileM, "plan tables count tiles of kTileM rows");
 
@@ -198,41 +201,6 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                : "memory");
 }
 
-// 32 lanes x 32 columns of 32-bit from TMEM, waited on before returning.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
-      "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
-      "%30, %31}, [%32];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
-        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
-        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr)
-      : "memory");
-}
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-      : "memory");
-}
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, "
-      "%29, %30, %31, %32};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
-      "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]),
-      "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]),
-      "r"(r[30]), "r"(r[31])
-      : "memory");
-}
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -251,7 +219,83 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 
 // ------------------------------------------------------------------ kernel --
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// Row max over the first `valid` of 128 scores (valid == 128: no masking).
+template <bool kFull>
+__device__ __forceinline__ float row_max(const uint32_t (&s)[128], int valid) {
+  float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+  for (int e = 0; e < 128; e += 8) {
+    float x[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      x[u] = (kFull || e + u < valid) ? __uint_as_float(s[e + u]) : -INFINITY;
+    m0 = fmax3(m0, x[0], x[1]);
+    m1 = fmax3(m1, x[2], x[3]);
+    m2 = fmax3(m2, x[4], x[5]);
+    m3 = fmax3(m3, x[6], x[7]);
+  }
+  return fmaxf(fmax3(m0, m1, m2), m3);
+}
+
+// p = 2^(s*scale_log2 - m) for the valid columns (0 elsewhere), packed to
+// bf16 pairs; returns the fp32 row sum of p.
+template <bool kFull>
+__device__ __forceinline__ float row_exp(const uint32_t (&s)[128], int valid, float scale_log2, float m,
+                                         uint32_t (&pk)[64]) {
+  const uint64_t sc = f2_pack(scale_log2, scale_log2);
+  const uint64_t nm = f2_pack(-m, -m);
+  uint64_t acc[4] = {0, 0, 0, 0};
+#pragma unroll
+  for (int e = 0; e < 64; ++e) {
+    float x0, x1;
+    f2_unpack(ffma2(f2_pack(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1])), sc, nm), x0, x1);
+    float p0 = ex2(x0), p1 = ex2(x1);
+    if (!kFull) {
+      p0 = 2 * e < valid ? p0 : 0.f;
+      p1 = 2 * e + 1 < valid ? p1 : 0.f;
+    }
+    acc[e & 3] = fadd2(acc[e & 3], f2_pack(p0, p1));
+    pk[e] = pack_bf16(p0, p1);
+  }
+  float a0, a1, b0, b1, c0, c1, d0, d1;
+  f2_unpack(fadd2(acc[0], acc[1]), a0, a1);
+  f2_unpack(fadd2(acc[2], acc[3]), b0, b1);
+  (void)c0; (void)c1; (void)d0; (void)d1;
+  return (a0 + a1) + (b0 + b1);
+}
+
 template <int HD>
+// 10 warps put 3 warps on one SM sub-partition (16K registers each), which
+// caps a thread at 168 registers.
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_qt,
@@ -306,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   if (bars->abort_flag) return;
-  if (warp == 2) {
+  if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_addr(&bars->tmem_base)),
                  "r"(kTmemCols)
@@ -318,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
-  if (warp == 0) {
+  if (warp == kProducerWarp) {
     // ======================= TMA producer ===============================
     if (lane == 0) {
       int issued_k = 0, issued_v = 0;
@@ -360,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (u >= 0) drain_wait(bar(bars->v_full[u & 1]), (u >> 1) & 1);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == kMmaWarp) {
     // ======================= MMA issuer =================================
     if (lane == 0) {
       constexpr uint32_t kIdescQK = idesc_bf16(kBM, kBN, false);
@@ -419,9 +463,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(bar(bars->mma_done));
       drain_wait(bar(bars->mma_done), 0);
     }
-  } else if (warp >= 4) {
-    // ======================= softmax + epilogue =========================
-    const int i = (warp - 4) >> 2;  // query tile of this warpgroup
+    __syncwarp();
+  } else {
+    // ======================= softmax + epilogue (warps 0-7) =============
+    const int i = warp >> 2;        // query tile of this warpgroup
     const int quarter = warp & 3;   // TMEM lanes 32*quarter .. +31
     const int r = quarter * 32 + lane;
     if (i < nq) {
@@ -436,49 +481,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         good = __all_sync(0xffffffffu, wait_phase(bs, j & 1, abort_flag, p.status));
         if (!good) break;
         tc_fence_after();
-        uint32_t s[32];
-        float mx = -INFINITY;
-#pragma unroll 1
-        for (int c = 0; c < kBN / 32; ++c) {
-          tmem_ld32(tS + c * 32, s);
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (c * 32 + e < valid) mx = fmaxf(mx, __uint_as_float(s[e]));
-        }
-        mx *= p.scale_log2;
+        uint32_t s[128];
+        tmem_ld_x128(tS, s);
+        const bool full = valid == kBN;
+        const float mx = (full ? row_max<true>(s, valid) : row_max<false>(s, valid)) * p.scale_log2;
+        // Running max with a lazy rescale: O and l move to a new max only
+        // when some row's max grew by more than 2^8; otherwise the stale max
+        // keeps every p <= 2^8, which fp32 and bf16 hold exactly enough, and
+        // the final O / l is unchanged.
+        bool rescale = false;
+        float alpha = 1.f;
         if (j == 0) {
           m_run = mx;
         } else if (__any_sync(0xffffffffu, mx > m_run + 8.f)) {
           const float m_new = fmaxf(m_run, mx);
-          const float alpha = ex2(m_run - m_new);
+          alpha = ex2(m_run - m_new);
           l_run *= alpha;
           m_run = m_new;
-#pragma unroll 1
-          for (int c = 0; c < HD / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tO + c * 32, o);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(tO + c * 32, o);
-          }
+          rescale = true;
         }
-        float sum = 0.f;
-#pragma unroll 1
-        for (int c = 0; c < kBN / 32; ++c) {
-          tmem_ld32(tS + c * 32, s);
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const float p0 = (c * 32 + e < valid) ? ex2(fmaf(__uint_as_float(s[e]), p.scale_log2, -m_run)) : 0.f;
-            const float p1 =
-                (c * 32 + e + 1 < valid) ? ex2(fmaf(__uint_as_float(s[e + 1]), p.scale_log2, -m_run)) : 0.f;
-            sum += p0 + p1;
-            pk[e >> 1] = pack_bf16(p0, p1);
-          }
-          // P (bf16, 2 per column) overwrites S columns already consumed.
-          tmem_st16(tS + c * 16, pk);
+        {
+          uint32_t pk[64];
+          l_run += full ? row_exp<true>(s, valid, p.scale_log2, m_run, pk)
+                        : row_exp<false>(s, valid, p.scale_log2, m_run, pk);
+          // P (bf16, 2 per column) overwrites S columns 0..63, already read.
+          tmem_st_x64(tS, pk);
         }
-        l_run += sum;
+        if (rescale) {
+          // O += P V of the previous tile has completed: this tile's S was
+          // committed after it.
+          uint32_t o[HD];
+          tmem_ld_x128_or_64<HD>(tO, o);
+          const uint64_t a2 = f2_pack(alpha, alpha);
+#pragma unroll
+          for (int e = 0; e < HD; e += 2) {
+            float x0, x1;
+            f2_unpack(fmul2(f2_pack(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), a2), x0, x1);
+            o[e] = __float_as_uint(x0);
+            o[e + 1] = __float_as_uint(x1);
+          }
+          tmem_st_x128_or_64<HD>(tO, o);
+        }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(bp);
@@ -488,42 +531,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const int t = t0 + i;
         const float inv_l = 1.f / l_run;
+        uint32_t o[HD];
+        tmem_ld_x128_or_64<HD>(tO, o);
         if (t < vt) {
           const int tok = t * kBM + r;
-          const bool live = tok < n_w;
-          __nv_bfloat16* dst =
-              live ? p.o_vid + static_cast<int64_t>(__ldg(p.ids + a + tok)) * p.o_stride + h * HD : nullptr;
-#pragma unroll 1
-          for (int c = 0; c < HD / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tO + c * 32, o);
-            if (live) {
-              uint32_t pk[16];
+          if (tok < n_w) {
+            __nv_bfloat16* dst = p.o_vid + static_cast<int64_t>(__ldg(p.ids + a + tok)) * p.o_stride + h * HD;
+            uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-              for (int e = 0; e < 32; e += 2)
-                pk[e >> 1] = pack_bf16(__uint_as_float(o[e]) * inv_l, __uint_as_float(o[e + 1]) * inv_l);
-              uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+            for (int q4 = 0; q4 < HD / 8; ++q4) {
+              uint32_t pk4[4];
 #pragma unroll
-              for (int q4 = 0; q4 < 4; ++q4)
-                d4[q4] = make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+              for (int u = 0; u < 4; ++u)
+                pk4[u] = pack_bf16(__uint_as_float(o[8 * q4 + 2 * u]) * inv_l,
+                                   __uint_as_float(o[8 * q4 + 2 * u + 1]) * inv_l);
+              d4[q4] = make_uint4(pk4[0], pk4[1], pk4[2], pk4[3]);
             }
           }
         } else {
           const int lt = (t - vt) * kBM + r;
-          const bool live = lt < p.L;
-          float* dst = live ? p.partial + ((static_cast<int64_t>(w) * p.L + lt) * p.heads + h) * HD : nullptr;
-#pragma unroll 1
-          for (int c = 0; c < HD / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tO + c * 32, o);
-            if (live) {
-              float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+          if (lt < p.L) {
+            float4* d4 = reinterpret_cast<float4*>(p.partial + ((static_cast<int64_t>(w) * p.L + lt) * p.heads + h) * HD);
 #pragma unroll
-              for (int q4 = 0; q4 < 8; ++q4)
-                d4[q4] = make_float4(__uint_as_float(o[4 * q4]) * inv_l, __uint_as_float(o[4 * q4 + 1]) * inv_l,
-                                     __uint_as_float(o[4 * q4 + 2]) * inv_l,
-                                     __uint_as_float(o[4 * q4 + 3]) * inv_l);
-            }
+            for (int q4 = 0; q4 < HD / 4; ++q4)
+              d4[q4] = make_float4(__uint_as_float(o[4 * q4]) * inv_l, __uint_as_float(o[4 * q4 + 1]) * inv_l,
+                                   __uint_as_float(o[4 * q4 + 2]) * inv_l, __uint_as_float(o[4 * q4 + 3]) * inv_l);
           }
         }
       }
@@ -532,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 2) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
                  : "memory");
