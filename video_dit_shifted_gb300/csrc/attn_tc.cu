@@ -120,12 +120,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
-// Bounded wait for the phase with the given parity.  Returns false if the
-// CTA is aborting (flag set by any thread) or this wait expired (then it
-// sets the flag and the status word).
-__device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                        int* status) {
-  if (mbar_try_wait(bar, parity)) return true;
+// Slow path of wait_phase: poll with a time limit.  Out of line, so that
+// the hot path stays a single try_wait (a call costs ~200 cycles of
+// register save/restore, which the MMA issue loop cannot afford).
+__device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                             int* status) {
   const uint64_t t0 = globaltimer();
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -138,6 +137,15 @@ __device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile 
       }
     }
   }
+}
+
+// Bounded wait for the phase with the given parity.  Returns false if the
+// CTA is aborting (flag set by any thread) or this wait expired (then it
+// sets the flag and the status word).
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                           int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_phase_slow(bar, parity, abort_flag, status);
 }
 
 // Bounded wait that ignores the abort flag (used while draining).
