@@ -36,6 +36,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstring>
 
 #include "attn_internal.h"
@@ -68,9 +69,9 @@ struct Cfg {
 constexpr int kSmemBytes = Cfg<128>::kBar + 256 + 1024;
 
 struct Barriers {
-  uint64_t q_full;
+  uint64_t q_full, q_empty;
   uint64_t k_full[2], v_full[2], k_empty[2], v_empty[2];
-  uint64_t s_full[2], p_full[2], o_full[2];
+  uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort_flag;
@@ -82,7 +83,7 @@ struct TcParams {
   const int32_t* ids;
   const int32_t* pair_off;  // pair_off[text_tiles & 1]
   int pair_add;             // text_tiles >> 1
-  int nwin, L, heads, text_tiles;
+  int nwin, L, heads, text_tiles, total_pairs;
   __nv_bfloat16* o_vid;
   int64_t o_stride;  // elements
   float* partial;
@@ -301,9 +302,38 @@ __device__ __forceinline__ float row_exp(const uint32_t (&s)[128], int valid, fl
   return (a0 + a1) + (b0 + b1);
 }
 
-template <int HD>
+// One work item: a pair of 128-row query tiles of one (window, head).
+struct Item {
+  int h, w, a, n_w, vt, nkv, t0, nq;
+};
+
+__device__ __forceinline__ Item decode_item(const TcParams& p, int it) {
+  Item x;
+  const int pidx = it % p.total_pairs;
+  x.h = it / p.total_pairs;
+  int lo = 0, hi = p.nwin - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(p.pair_off + mid) + mid * p.pair_add <= pidx) lo = mid; else hi = mid - 1;
+  }
+  x.w = lo;
+  x.a = __ldg(p.win_off + lo);
+  x.n_w = __ldg(p.win_off + lo + 1) - x.a;
+  x.vt = (x.n_w + kBN - 1) / kBN;  // video tiles (queries and keys alike)
+  x.nkv = x.vt + p.text_tiles;
+  x.t0 = 2 * (pidx - (__ldg(p.pair_off + lo) + lo * p.pair_add));
+  x.nq = min(2, x.nkv - x.t0);
+  return x;
+}
+
+// Persistent: CTA b processes items b, b + gridDim.x, b + 2*gridDim.x, ...
+// (items = query-tile pairs x heads, pairs of one (window, head) adjacent,
+// so the CTAs working at the same time share K/V tiles through L2).  Every
+// role walks the same item sequence; barrier phases follow running counters
+// that all roles advance identically.
 // 10 warps put 3 warps on one SM sub-partition (16K registers each), which
 // caps a thread at 168 registers.
+template <int HD>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_qt,
@@ -316,31 +346,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = smem_raw + (base - raw);
   Barriers* bars = reinterpret_cast<Barriers*>(smem + C::kBar);
   volatile int* abort_flag = &bars->abort_flag;
-
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.y;
+  const int n_items = p.total_pairs * p.heads;
 
-  // ---- work item: which window, which pair of query tiles --------------
-  const int pidx = blockIdx.x;
-  int lo = 0, hi = p.nwin - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(p.pair_off + mid) + mid * p.pair_add <= pidx) lo = mid; else hi = mid - 1;
-  }
-  const int w = lo;
-  const int a = __ldg(p.win_off + w);
-  const int n_w = __ldg(p.win_off + w + 1) - a;
-  const int vt = (n_w + kBN - 1) / kBN;  // video tiles (queries and keys alike)
-  const int tt = p.text_tiles;
-  const int nkv = vt + tt;
-  const int t0 = 2 * (pidx - (__ldg(p.pair_off + w) + w * p.pair_add));
-  const int nq = min(2, nkv - t0);
-
-  const uint32_t bq_full = smem_addr(&bars->q_full);
+  const uint32_t bq_full = smem_addr(&bars->q_full), bq_empty = smem_addr(&bars->q_empty);
   auto bar = [](uint64_t& b) { return smem_addr(&b); };
 
   if (threadIdx.x == 0) {
     mbar_init(bq_full, 1);
+    mbar_init(bq_empty, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(bars->k_full[s]), 1);
       mbar_init(bar(bars->v_full[s]), 1);
@@ -349,6 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(bars->s_full[s]), 1);
       mbar_init(bar(bars->p_full[s]), 128);
       mbar_init(bar(bars->o_full[s]), 1);
+      mbar_init(bar(bars->o_empty[s]), 128);
     }
     mbar_init(bar(bars->mma_done), 1);
     // A CTA of this launch already failed: skip the work so that a broken
@@ -373,42 +388,49 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kProducerWarp) {
     // ======================= TMA producer ===============================
     if (lane == 0) {
-      int issued_k = 0, issued_v = 0;
+      int gk = 0, gv = 0;  // K and V tiles issued so far (ring positions)
+      int k = 0;           // items whose Q load was issued
       bool good = true;
-      mbar_expect_tx(bq_full, nq * C::kTileBytes);
-      for (int i = 0; i < nq; ++i) {
-        const int t = t0 + i;
-        const CUtensorMap* map = t < vt ? &tm_q : &tm_qt;
-        const int row = t < vt ? a + t * kBM : (t - vt) * kBM;
-        for (int hf = 0; hf < C::kHalves; ++hf)
-          tma_load_2d(base + C::kQ + i * C::kTileBytes + hf * C::kBoxBytes, map, bq_full,
-                      h * HD + hf * 64, row);
-      }
-      for (int j = 0; j < nkv && good; ++j) {
-        const int s = j & 1;
-        const bool vid = j < vt;
-        const int row = vid ? a + j * kBN : (j - vt) * kBN;
-        if (j >= 2 && !(good = wait_phase(bar(bars->k_empty[s]), ((j >> 1) - 1) & 1, abort_flag, p.status)))
-          break;
-        mbar_expect_tx(bar(bars->k_full[s]), C::kTileBytes);
-        for (int hf = 0; hf < C::kHalves; ++hf)
-          tma_load_2d(base + C::kK + s * C::kTileBytes + hf * C::kBoxBytes, vid ? &tm_k : &tm_kt,
-                      bar(bars->k_full[s]), h * HD + hf * 64, row);
-        ++issued_k;
-        if (j >= 2 && !(good = wait_phase(bar(bars->v_empty[s]), ((j >> 1) - 1) & 1, abort_flag, p.status)))
-          break;
-        mbar_expect_tx(bar(bars->v_full[s]), C::kTileBytes);
-        for (int hf = 0; hf < C::kHalves; ++hf)
-          tma_load_2d(base + C::kV + s * C::kTileBytes + hf * C::kBoxBytes, vid ? &tm_v : &tm_vt,
-                      bar(bars->v_full[s]), h * HD + hf * 64, row);
-        ++issued_v;
+      for (int it = blockIdx.x; it < n_items && good; it += gridDim.x) {
+        const Item x = decode_item(p, it);
+        // Q smem is free once the previous item's last Q K^T has completed.
+        if (k > 0 && !(good = wait_phase(bq_empty, (k - 1) & 1, abort_flag, p.status))) break;
+        mbar_expect_tx(bq_full, x.nq * C::kTileBytes);
+        for (int i = 0; i < x.nq; ++i) {
+          const int t = x.t0 + i;
+          const CUtensorMap* map = t < x.vt ? &tm_q : &tm_qt;
+          const int row = t < x.vt ? x.a + t * kBM : (t - x.vt) * kBM;
+          for (int hf = 0; hf < C::kHalves; ++hf)
+            tma_load_2d(base + C::kQ + i * C::kTileBytes + hf * C::kBoxBytes, map, bq_full,
+                        x.h * HD + hf * 64, row);
+        }
+        ++k;
+        for (int j = 0; j < x.nkv; ++j) {
+          const bool vid = j < x.vt;
+          const int row = vid ? x.a + j * kBN : (j - x.vt) * kBN;
+          const int s = gk & 1;
+          if (gk >= 2 && !(good = wait_phase(bar(bars->k_empty[s]), ((gk >> 1) - 1) & 1, abort_flag, p.status)))
+            break;
+          mbar_expect_tx(bar(bars->k_full[s]), C::kTileBytes);
+          for (int hf = 0; hf < C::kHalves; ++hf)
+            tma_load_2d(base + C::kK + s * C::kTileBytes + hf * C::kBoxBytes, vid ? &tm_k : &tm_kt,
+                        bar(bars->k_full[s]), x.h * HD + hf * 64, row);
+          ++gk;
+          if (gv >= 2 && !(good = wait_phase(bar(bars->v_empty[s]), ((gv >> 1) - 1) & 1, abort_flag, p.status)))
+            break;
+          mbar_expect_tx(bar(bars->v_full[s]), C::kTileBytes);
+          for (int hf = 0; hf < C::kHalves; ++hf)
+            tma_load_2d(base + C::kV + s * C::kTileBytes + hf * C::kBoxBytes, vid ? &tm_v : &tm_vt,
+                        bar(bars->v_full[s]), x.h * HD + hf * 64, row);
+          ++gv;
+        }
       }
       if (*abort_flag) {
         // Let every copy this thread started land before the CTA exits.
-        drain_wait(bq_full, 0);
-        for (int u = issued_k - 2; u < issued_k; ++u)
+        if (k > 0) drain_wait(bq_full, (k - 1) & 1);
+        for (int u = gk - 2; u < gk; ++u)
           if (u >= 0) drain_wait(bar(bars->k_full[u & 1]), (u >> 1) & 1);
-        for (int u = issued_v - 2; u < issued_v; ++u)
+        for (int u = gv - 2; u < gv; ++u)
           if (u >= 0) drain_wait(bar(bars->v_full[u & 1]), (u >> 1) & 1);
       }
     }
@@ -436,36 +458,56 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ts(colO[i], colS[i] + kk * 8, sw128_desc(vb + kk * 2048, C::kBoxBytes, 1024), kIdescPV,
                  (!first || kk > 0) ? 1u : 0u);
       };
-      bool good = wait_phase(bq_full, 0, abort_flag, p.status) &&
-                  wait_phase(bar(bars->k_full[0]), 0, abort_flag, p.status);
-      if (good) {
+      int g = 0;                  // K/V tiles consumed
+      int k = 0;                  // items
+      int cs[2] = {0, 0};         // tiles per softmax warpgroup (s_full / p_full phases)
+      int co[2] = {0, 0};         // items per softmax warpgroup (o_full / o_empty phases)
+      bool good = true;
+      for (int it = blockIdx.x; it < n_items && good; it += gridDim.x, ++k) {
+        const Item x = decode_item(p, it);
+        if (!(good = wait_phase(bq_full, k & 1, abort_flag, p.status) &&
+                     wait_phase(bar(bars->k_full[g & 1]), (g >> 1) & 1, abort_flag, p.status)))
+          break;
         tc_fence_after();
-        for (int i = 0; i < nq; ++i) {
-          issue_qk(i, 0);
+        for (int i = 0; i < x.nq; ++i) {
+          issue_qk(i, g & 1);
           mma_commit(bar(bars->s_full[i]));
         }
-        mma_commit(bar(bars->k_empty[0]));
-      }
-      for (int j = 0; j < nkv && good; ++j) {
-        const int s = j & 1, sn = (j + 1) & 1;
-        const bool more = j + 1 < nkv;
-        if (!(good = wait_phase(bar(bars->v_full[s]), (j >> 1) & 1, abort_flag, p.status))) break;
-        for (int i = 0; i < nq; ++i) {
-          if (!(good = wait_phase(bar(bars->p_full[i]), j & 1, abort_flag, p.status))) break;
-          tc_fence_after();
-          issue_pv(i, s, j == 0);
-          if (!more) mma_commit(bar(bars->o_full[i]));
-          if (more) {
-            if (i == 0 && !(good = wait_phase(bar(bars->k_full[sn]), ((j + 1) >> 1) & 1, abort_flag, p.status)))
+        mma_commit(bar(bars->k_empty[g & 1]));
+        if (x.nkv == 1) mma_commit(bq_empty);
+        for (int j = 0; j < x.nkv && good; ++j) {
+          const int s = (g + j) & 1, sn = (g + j + 1) & 1;
+          const bool more = j + 1 < x.nkv;
+          if (!(good = wait_phase(bar(bars->v_full[s]), ((g + j) >> 1) & 1, abort_flag, p.status))) break;
+          for (int i = 0; i < x.nq; ++i) {
+            if (!(good = wait_phase(bar(bars->p_full[i]), (cs[i] + j) & 1, abort_flag, p.status))) break;
+            // O_i is overwritten by this item's first P V: the previous
+            // item's epilogue must have read it out.
+            if (j == 0 && co[i] > 0 &&
+                !(good = wait_phase(bar(bars->o_empty[i]), (co[i] - 1) & 1, abort_flag, p.status)))
               break;
             tc_fence_after();
-            issue_qk(i, sn);
-            mma_commit(bar(bars->s_full[i]));
+            issue_pv(i, s, j == 0);
+            if (!more) mma_commit(bar(bars->o_full[i]));
+            if (more) {
+              if (i == 0 &&
+                  !(good = wait_phase(bar(bars->k_full[sn]), ((g + j + 1) >> 1) & 1, abort_flag, p.status)))
+                break;
+              tc_fence_after();
+              issue_qk(i, sn);
+              mma_commit(bar(bars->s_full[i]));
+            }
           }
+          if (!good) break;
+          mma_commit(bar(bars->v_empty[s]));
+          if (more) mma_commit(bar(bars->k_empty[sn]));
+          if (j + 2 == x.nkv) mma_commit(bq_empty);  // the Q K^T just issued was the item's last
         }
-        if (!good) break;
-        mma_commit(bar(bars->v_empty[s]));
-        if (more) mma_commit(bar(bars->k_empty[sn]));
+        for (int i = 0; i < x.nq; ++i) {
+          cs[i] += x.nkv;
+          co[i] += 1;
+        }
+        g += x.nkv;
       }
       // All MMAs this thread issued must finish before TMEM is freed.
       mma_commit(bar(bars->mma_done));
@@ -477,16 +519,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int i = warp >> 2;        // query tile of this warpgroup
     const int quarter = warp & 3;   // TMEM lanes 32*quarter .. +31
     const int r = quarter * 32 + lane;
-    if (i < nq) {
-      const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-      const uint32_t tS = tmem + (i == 0 ? C::kColS0 : C::kColS1) + lane_off;
-      const uint32_t tO = tmem + (i == 0 ? C::kColO0 : C::kColO1) + lane_off;
-      const uint32_t bs = bar(bars->s_full[i]), bp = bar(bars->p_full[i]);
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tS = tmem + (i == 0 ? C::kColS0 : C::kColS1) + lane_off;
+    const uint32_t tO = tmem + (i == 0 ? C::kColO0 : C::kColO1) + lane_off;
+    const uint32_t bs = bar(bars->s_full[i]), bp = bar(bars->p_full[i]);
+    int cs = 0, co = 0;
+    bool good = true;
+    for (int it = blockIdx.x; it < n_items && good; it += gridDim.x) {
+      const Item x = decode_item(p, it);
+      if (i >= x.nq) continue;
       float m_run = 0.f, l_run = 0.f;
-      bool good = true;
-      for (int j = 0; j < nkv; ++j) {
-        const int valid = j < vt ? min(kBN, n_w - j * kBN) : min(kBN, p.L - (j - vt) * kBN);
-        good = __all_sync(0xffffffffu, wait_phase(bs, j & 1, abort_flag, p.status));
+      for (int j = 0; j < x.nkv; ++j) {
+        const int valid = j < x.vt ? min(kBN, x.n_w - j * kBN) : min(kBN, p.L - (j - x.vt) * kBN);
+        good = __all_sync(0xffffffffu, wait_phase(bs, (cs + j) & 1, abort_flag, p.status));
         if (!good) break;
         tc_fence_after();
         uint32_t s[128];
@@ -534,37 +579,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(bp);
       }
-      if (good) good = __all_sync(0xffffffffu, wait_phase(bar(bars->o_full[i]), 0, abort_flag, p.status));
-      if (good) {
-        tc_fence_after();
-        const int t = t0 + i;
-        const float inv_l = 1.f / l_run;
-        uint32_t o[HD];
-        tmem_ld_x128_or_64<HD>(tO, o);
-        if (t < vt) {
-          const int tok = t * kBM + r;
-          if (tok < n_w) {
-            __nv_bfloat16* dst = p.o_vid + static_cast<int64_t>(__ldg(p.ids + a + tok)) * p.o_stride + h * HD;
-            uint4* d4 = reinterpret_cast<uint4*>(dst);
+      if (!good) break;
+      cs += x.nkv;
+      good = __all_sync(0xffffffffu, wait_phase(bar(bars->o_full[i]), co & 1, abort_flag, p.status));
+      if (!good) break;
+      tc_fence_after();
+      uint32_t o[HD];
+      tmem_ld_x128_or_64<HD>(tO, o);
+      // O is in registers: the MMA may start the next item's P V.
+      tc_fence_before();
+      mbar_arrive(bar(bars->o_empty[i]));
+      ++co;
+      const int t = x.t0 + i;
+      const float inv_l = 1.f / l_run;
+      if (t < x.vt) {
+        const int tok = t * kBM + r;
+        if (tok < x.n_w) {
+          __nv_bfloat16* dst = p.o_vid + static_cast<int64_t>(__ldg(p.ids + x.a + tok)) * p.o_stride + x.h * HD;
+          uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-            for (int q4 = 0; q4 < HD / 8; ++q4) {
-              uint32_t pk4[4];
+          for (int q4 = 0; q4 < HD / 8; ++q4) {
+            uint32_t pk4[4];
 #pragma unroll
-              for (int u = 0; u < 4; ++u)
-                pk4[u] = pack_bf16(__uint_as_float(o[8 * q4 + 2 * u]) * inv_l,
-                                   __uint_as_float(o[8 * q4 + 2 * u + 1]) * inv_l);
-              d4[q4] = make_uint4(pk4[0], pk4[1], pk4[2], pk4[3]);
-            }
+            for (int u = 0; u < 4; ++u)
+              pk4[u] = pack_bf16(__uint_as_float(o[8 * q4 + 2 * u]) * inv_l,
+                                 __uint_as_float(o[8 * q4 + 2 * u + 1]) * inv_l);
+            d4[q4] = make_uint4(pk4[0], pk4[1], pk4[2], pk4[3]);
           }
-        } else {
-          const int lt = (t - vt) * kBM + r;
-          if (lt < p.L) {
-            float4* d4 = reinterpret_cast<float4*>(p.partial + ((static_cast<int64_t>(w) * p.L + lt) * p.heads + h) * HD);
+        }
+      } else {
+        const int lt = (t - x.vt) * kBM + r;
+        if (lt < p.L) {
+          float4* d4 = reinterpret_cast<float4*>(p.partial + ((static_cast<int64_t>(x.w) * p.L + lt) * p.heads + x.h) * HD);
 #pragma unroll
-            for (int q4 = 0; q4 < HD / 4; ++q4)
-              d4[q4] = make_float4(__uint_as_float(o[4 * q4]) * inv_l, __uint_as_float(o[4 * q4 + 1]) * inv_l,
-                                   __uint_as_float(o[4 * q4 + 2]) * inv_l, __uint_as_float(o[4 * q4 + 3]) * inv_l);
-          }
+          for (int q4 = 0; q4 < HD / 4; ++q4)
+            d4[q4] = make_float4(__uint_as_float(o[4 * q4]) * inv_l, __uint_as_float(o[4 * q4 + 1]) * inv_l,
+                                 __uint_as_float(o[4 * q4 + 2]) * inv_l, __uint_as_float(o[4 * q4 + 3]) * inv_l);
         }
       }
     }
@@ -632,6 +682,7 @@ int launch(const AttnCall& c) {
   p.L = c.L;
   p.heads = c.heads;
   p.text_tiles = c.text_tiles;
+  p.total_pairs = c.total_pairs;
   p.o_vid = static_cast<__nv_bfloat16*>(c.o_vid);
   p.o_stride = c.o_stride_B / 2;
   p.partial = c.partial;
@@ -641,7 +692,15 @@ int launch(const AttnCall& c) {
   if (int rc = cuda_check(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes),
                           "cudaFuncSetAttribute(attn_tc_kernel)"))
     return rc;
-  dim3 grid(static_cast<unsigned>(c.total_pairs), static_cast<unsigned>(c.heads));
+  int dev = 0, sms = 0;
+  if (int rc = cuda_check(cudaGetDevice(&dev), "cudaGetDevice")) return rc;
+  if (int rc = cuda_check(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev),
+                          "cudaDeviceGetAttribute"))
+    return rc;
+  // Persistent: one CTA per SM (shared memory and TMEM allow no second).
+  const int64_t items = static_cast<int64_t>(c.total_pairs) * c.heads;
+  if (items > 0x7fffffff) return fail(WP_EUNSUPPORTED, "too many work items");
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(items, sms));
   kern<<<grid, kThreads, kSmemBytes, c.stream>>>(mq, mk, mv, mqt, mkt, mvt, p);
   return cuda_check(cudaGetLastError(), "attn_tc_kernel launch");
 }
