@@ -38,6 +38,7 @@
 
 #include <algorithm>
 #include <cstring>
+#include <type_traits>
 
 #include "attn_internal.h"
 #include "tmem_io.cuh"
@@ -439,73 +440,84 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdescQK = idesc_bf16(kBM, kBN, false);
       constexpr uint32_t kIdescPV = idesc_bf16(kBM, HD, true);
-      const uint32_t colS[2] = {tmem + C::kColS0, tmem + C::kColS1};
-      const uint32_t colO[2] = {tmem + C::kColO0, tmem + C::kColO1};
+      // Descriptors are built once per tile and advanced by constant offsets
+      // (the start-address field holds address >> 4 and never carries out of
+      // its 14 bits for a shared-memory address), keeping the issue loop short.
       auto issue_qk = [&](int i, int s) {
-        const uint32_t qa = base + C::kQ + i * C::kTileBytes;
-        const uint32_t kb = base + C::kK + s * C::kTileBytes;
+        const uint32_t dS = tmem + (i ? C::kColS1 : C::kColS0);
+        const uint64_t qd = sw128_desc(base + C::kQ + i * C::kTileBytes, 16, 1024);
+        const uint64_t kd = sw128_desc(base + C::kK + s * C::kTileBytes, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
-          mma_ss(colS[i], sw128_desc(qa + off, 16, 1024), sw128_desc(kb + off, 16, 1024), kIdescQK,
-                 kk > 0);
+          const uint32_t off16 = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
+          mma_ss(dS, qd + off16, kd + off16, kIdescQK, kk > 0);
         }
       };
       auto issue_pv = [&](int i, int s, bool first) {
-        const uint32_t vb = base + C::kV + s * C::kTileBytes;
+        const uint32_t dO = tmem + (i ? C::kColO1 : C::kColO0);
+        const uint32_t aP = tmem + (i ? C::kColS1 : C::kColS0);
+        const uint64_t vd = sw128_desc(base + C::kV + s * C::kTileBytes, C::kBoxBytes, 1024);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_ts(colO[i], colS[i] + kk * 8, sw128_desc(vb + kk * 2048, C::kBoxBytes, 1024), kIdescPV,
-                 (!first || kk > 0) ? 1u : 0u);
+          mma_ts(dO, aP + kk * 8, vd + ((kk * 2048) >> 4), kIdescPV, (!first || kk > 0) ? 1u : 0u);
       };
       int g = 0;                  // K/V tiles consumed
       int k = 0;                  // items
-      int cs[2] = {0, 0};         // tiles per softmax warpgroup (s_full / p_full phases)
-      int co[2] = {0, 0};         // items per softmax warpgroup (o_full / o_empty phases)
+      int cs0 = 0, cs1 = 0;       // tiles per softmax warpgroup (s_full / p_full phases)
+      int co0 = 0, co1 = 0;       // items per softmax warpgroup (o_full / o_empty phases)
       bool good = true;
+      // One query tile's share of step j: O_i += P_i V_j, then S_i = Q_i K_{j+1}^T.
+      // The tile index is a compile-time constant so that every phase counter
+      // and TMEM address stays in registers.
+      auto tile_step = [&](auto I, int j, int s, int sn, bool more, int cs, int co) -> bool {
+        constexpr int i = decltype(I)::value;
+        if (!wait_phase(bar(bars->p_full[i]), (cs + j) & 1, abort_flag, p.status)) return false;
+        // O_i is overwritten by this item's first P V: the previous item's
+        // epilogue must have read it out.
+        if (j == 0 && co > 0 && !wait_phase(bar(bars->o_empty[i]), (co - 1) & 1, abort_flag, p.status))
+          return false;
+        tc_fence_after();
+        issue_pv(i, s, j == 0);
+        if (more) {
+          issue_qk(i, sn);
+          mma_commit(bar(bars->s_full[i]));
+        } else {
+          mma_commit(bar(bars->o_full[i]));
+        }
+        return true;
+      };
       for (int it = blockIdx.x; it < n_items && good; it += gridDim.x, ++k) {
         const Item x = decode_item(p, it);
         if (!(good = wait_phase(bq_full, k & 1, abort_flag, p.status) &&
                      wait_phase(bar(bars->k_full[g & 1]), (g >> 1) & 1, abort_flag, p.status)))
           break;
         tc_fence_after();
-        for (int i = 0; i < x.nq; ++i) {
-          issue_qk(i, g & 1);
-          mma_commit(bar(bars->s_full[i]));
+        issue_qk(0, g & 1);
+        mma_commit(bar(bars->s_full[0]));
+        if (x.nq > 1) {
+          issue_qk(1, g & 1);
+          mma_commit(bar(bars->s_full[1]));
         }
         mma_commit(bar(bars->k_empty[g & 1]));
         if (x.nkv == 1) mma_commit(bq_empty);
-        for (int j = 0; j < x.nkv && good; ++j) {
+        for (int j = 0; j < x.nkv; ++j) {
           const int s = (g + j) & 1, sn = (g + j + 1) & 1;
           const bool more = j + 1 < x.nkv;
+          // V_j for this step and K_{j+1} for the next: usually landed long ago.
           if (!(good = wait_phase(bar(bars->v_full[s]), ((g + j) >> 1) & 1, abort_flag, p.status))) break;
-          for (int i = 0; i < x.nq; ++i) {
-            if (!(good = wait_phase(bar(bars->p_full[i]), (cs[i] + j) & 1, abort_flag, p.status))) break;
-            // O_i is overwritten by this item's first P V: the previous
-            // item's epilogue must have read it out.
-            if (j == 0 && co[i] > 0 &&
-                !(good = wait_phase(bar(bars->o_empty[i]), (co[i] - 1) & 1, abort_flag, p.status)))
-              break;
-            tc_fence_after();
-            issue_pv(i, s, j == 0);
-            if (!more) mma_commit(bar(bars->o_full[i]));
-            if (more) {
-              if (i == 0 &&
-                  !(good = wait_phase(bar(bars->k_full[sn]), ((g + j + 1) >> 1) & 1, abort_flag, p.status)))
-                break;
-              tc_fence_after();
-              issue_qk(i, sn);
-              mma_commit(bar(bars->s_full[i]));
-            }
-          }
-          if (!good) break;
+          if (more && !(good = wait_phase(bar(bars->k_full[sn]), ((g + j + 1) >> 1) & 1, abort_flag, p.status)))
+            break;
+          if (!(good = tile_step(std::integral_constant<int, 0>{}, j, s, sn, more, cs0, co0))) break;
+          if (x.nq > 1 && !(good = tile_step(std::integral_constant<int, 1>{}, j, s, sn, more, cs1, co1))) break;
           mma_commit(bar(bars->v_empty[s]));
           if (more) mma_commit(bar(bars->k_empty[sn]));
           if (j + 2 == x.nkv) mma_commit(bq_empty);  // the Q K^T just issued was the item's last
         }
-        for (int i = 0; i < x.nq; ++i) {
-          cs[i] += x.nkv;
-          co[i] += 1;
+        cs0 += x.nkv;
+        co0 += 1;
+        if (x.nq > 1) {
+          cs1 += x.nkv;
+          co1 += 1;
         }
         g += x.nkv;
       }
