@@ -23,7 +23,9 @@
  *     one-line message (thread-local, valid until the next call on the same
  *     thread).
  *   - Device pointers are plain CUDA device addresses; the caller owns all
- *     device memory (the library never allocates device memory).  `stream`
+ *     device memory (the library never allocates device memory; the one
+ *     fixed array that wp_window_attn_static uses is part of the library's
+ *     device image).  `stream`
  *     is a cudaStream_t passed as void* (NULL = legacy default stream).  All
  *     device work is asynchronous on that stream.
  *   - Faults detected on the device (a bounded wait that expired, a failed
@@ -163,6 +165,38 @@ int wp_window_attn(const wp_plan* plan, int layout, int heads, int head_dim,
                    void* o_vid, int64_t o_vid_row_stride_B, void* o_txt,
                    void* workspace, size_t ws_bytes, float softmax_scale,
                    void* stream);
+
+/* wp_window_attn_static -- wp_window_attn for callers that cannot allocate
+ * device memory when they run attention (a runtime that owns a fixed memory
+ * pool and forbids allocation from plugins, a latency-bound loop that cannot
+ * afford the implicit device synchronisation of cudaMalloc, a caller with no
+ * allocator at hand).  The pages define nothing like it: it is a convenience
+ * of this library with no counterpart in the method.
+ * Same arguments, layout and results as wp_window_attn, minus the workspace:
+ * the scratch (status block + per-window text outputs) comes from one
+ * array of WP_STATIC_SCRATCH_BYTES bytes compiled into the library's device
+ * image, which every GPU that loads the library holds until the process
+ * exits.  The call allocates nothing and calls no allocating routine.
+ *   - Size limit: the call needs 256 + nwin*L*heads*head_dim*4 bytes of
+ *     scratch (wp_attn_workspace_bytes); larger requests return
+ *     WP_EUNSUPPORTED with a message, and nothing is launched.
+ *   - Set-up: the first call on each device looks up the array's device
+ *     address (cudaGetSymbolAddress) with that device current and remembers
+ *     it; make that first call before capturing any stream into a graph.
+ *   - Sharing: every call on a device uses the same array, which keeps the
+ *     last call's contents (the call clears what must start at zero).  Calls
+ *     whose work overlaps on the GPU (e.g. on two streams at once) race on
+ *     it: order them on one stream or synchronise between them.
+ *   - The device status word is not readable by the caller; a bounded wait
+ *     that expires still ends the kernel. */
+#define WP_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
+int wp_window_attn_static(const wp_plan* plan, int layout, int heads, int head_dim,
+                          int L, int dtype, const void* q, const void* k,
+                          const void* v, int64_t vid_row_stride_B,
+                          const void* qt, const void* kt, const void* vt,
+                          int64_t txt_row_stride_B, void* o_vid,
+                          int64_t o_vid_row_stride_B, void* o_txt,
+                          float softmax_scale, void* stream);
 
 /* wp_read_status -- copies the device status word of `workspace` to
  * *device_status (a wp_status value: WP_OK, WP_ETIMEOUT or WP_EDEVICE),

@@ -35,6 +35,9 @@ SIGNATURES = {
     "wp_window_attn": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int,
                                 _vp, _vp, _vp, _c_i64, _vp, _vp, _vp, _c_i64,
                                 _vp, _c_i64, _vp, _vp, _c_sz, ctypes.c_float, _vp]),
+    "wp_window_attn_static": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                       _vp, _vp, _vp, _c_i64, _vp, _vp, _vp, _c_i64,
+                                       _vp, _c_i64, _vp, ctypes.c_float, _vp]),
     "wp_read_status": (_c_int, [_vp, ctypes.POINTER(_c_int), _vp]),
     "wp_last_error": (ctypes.c_char_p, []),
     "wp_abi_version": (_c_int, []),
