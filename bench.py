@@ -308,6 +308,90 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_full_schedule(args):
+    """The full 32-layer schedule on T=30, H=90, W=160 (N=432000): layer l
+    runs window attention in the regular layout if l is even, else shifted;
+    between layers the packed qkv rows [N, 3, 24, 128] bf16 are re-laid out
+    into the next layer's order (31 transitions); the text output of every
+    layer is mean-reduced.  One step = all 32 layers."""
+    import video_dit_shifted_gb300 as vds
+    from video_dit_shifted_gb300 import schedule, synth
+    import __graft_entry__
+    __graft_entry__.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    T, H, W, heads, hd, L = 30, 90, 160, 24, 128, 256
+    plan = vds.Plan(T, H, W, 4, 3, 3, device=dev)
+    N = plan.N
+    layouts = schedule.layer_layouts(32)
+    trans = schedule.transitions(layouts)
+    x = synth.attention_inputs(N, L, heads, hd, torch.bfloat16, dev)
+    bufs = [x["vid_buf"], torch.empty_like(x["vid_buf"])]      # ping-pong, starts in REGULAR order
+    txt = x["txt_buf"]
+    o_vid = torch.empty((N, heads, hd), dtype=torch.bfloat16, device=dev)
+    o_txt = torch.empty((32, L, heads, hd), dtype=torch.bfloat16, device=dev)
+    ws = {l: vds.make_workspace(plan, l, heads, hd, L, vds.BF16, dev) for l in (vds.REGULAR, vds.SHIFTED)}
+    flops = {l: attn_flops(np.diff(plan.host_tables(l)[0]), heads, hd, L) for l in (vds.REGULAR, vds.SHIFTED)}
+    step_flops = sum(flops[l] for l in layouts)
+    row_B = bufs[0][0].numel() * 2
+    step_bytes = len(trans) * 2.0 * N * row_B
+
+    def step(ev=None):
+        cur = 0
+        for l, lay in enumerate(layouts):
+            b = bufs[cur]
+            if ev: ev[0].record()
+            vds.window_attn(plan, lay, b[:, 0], b[:, 1], b[:, 2], txt[:, 0], txt[:, 1], txt[:, 2], o_vid,
+                            o_txt[l], ws[lay])
+            if ev: ev[1].record(); ev[2].append((ev[0], ev[1]))
+            if l + 1 < len(layouts):
+                nxt = layouts[l + 1]
+                if ev: ev[3].record()
+                vds.permute(plan, bufs[cur].view(N, -1), bufs[1 - cur].view(N, -1), lay, nxt)
+                if ev: ev[4].record(); ev[5].append((ev[3], ev[4]))
+                cur = 1 - cur
+                if ev:
+                    ev[0], ev[1], ev[3], ev[4] = (torch.cuda.Event(enable_timing=True) for _ in range(4))
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    for l, w in ws.items():
+        assert vds.read_status(w) == 0
+    clocks = ClockSampler(0)
+    clocks.start()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    attn_pairs, perm_pairs = [], []
+    s.record()
+    for _ in range(args.steps):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)] + [attn_pairs] + \
+             [torch.cuda.Event(enable_timing=True) for _ in range(2)] + [perm_pairs]
+        step(ev)
+    e.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = s.elapsed_time(e) / args.steps
+    attn_ms = sum(a.elapsed_time(b) for a, b in attn_pairs) / args.steps
+    perm_ms = sum(a.elapsed_time(b) for a, b in perm_pairs) / args.steps
+    peaks, peak_src = load_peaks()
+    a_tf = step_flops / (attn_ms * 1e-3) / 1e12
+    gbs = step_bytes / (perm_ms * 1e-3) / 1e9
+    line = {"metric": METRIC, "value": step_flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "full schedule: 32 alternating regular/shifted layers (31 re-layouts of packed "
+                                   "qkv [N,3,24,128] bf16) on T=30 H=90 W=160 (N=432000), nt=4 nh=3 nw=3, "
+                                   "heads=24 head_dim=128, text L=256, text mean per layer",
+                       "l2": "inputs larger than L2: no flush"},
+            "attn_tflops": a_tf, "attn_frac_bf16_peak": a_tf / peaks["bf16_tflops"],
+            "attn_ms_per_step": attn_ms, "attn_tflop_per_step": step_flops / 1e12,
+            "relayout_gbs": gbs, "relayout_frac_hbm": gbs / peaks["hbm_gbs"], "relayout_ms_per_step": perm_ms,
+            "relayout_gb_per_step": step_bytes / 1e9, "peak_source": peak_src,
+            "gpu_launches": args.steps * (2 * len(layouts) + len(trans)), "clocks": clk}
+    print(json.dumps(line), flush=True)
+    plan.close()
+
+
 def run_ours(args):
     world, rank, local, pg = dist_setup(args)
     dev = torch.device("cuda", local)
@@ -393,7 +477,7 @@ def main():
     ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="1080p")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + ["full"], default="1080p")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--ref-step-s", type=float, default=4.0)
@@ -404,6 +488,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "full":
+        run_full_schedule(args)
     else:
         run_ours(args)
 

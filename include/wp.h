@@ -112,6 +112,38 @@ int wp_plan_host_tables(const wp_plan* plan, int layout, int32_t* win_off,
 int wp_plan_device_bytes(const wp_plan* plan, size_t* bytes);
 int wp_plan_upload(wp_plan* plan, void* dev_buf, size_t bytes, void* stream);
 
+/* Window -> rank assignment for running a layout on `world` devices
+ * (§Planner): windows taken by (-token count, window id), each placed on the
+ * rank with the smallest (assigned tokens, rank id); a rank lists its windows
+ * in ascending window id.  win_rank[nwin] receives each window's rank and
+ * rank_tokens[world] each rank's token count (either may be NULL).  Host
+ * only; WP_EINVAL for world < 1 or a bad layout. */
+int wp_plan_assign(const wp_plan* plan, int layout, int world, int32_t* win_rank,
+                   int64_t* rank_tokens);
+
+/* Plan A exchange between two layouts on `world` devices (§Plan A
+ * redistribution), seen from rank `rank`; host only.  With both layouts
+ * assigned as in wp_plan_assign and each rank's rows in its local order:
+ *   counts[world*world]  C[r*world + d] = rows rank d needs from rank r
+ *                        (row r = input split sizes of rank r, column d =
+ *                        output split sizes of rank d);
+ *   *exchange_required   1 if any row changes rank (then every rank must
+ *                        join the all-to-all), 0 if the switch is a local
+ *                        permutation (always the case for world == 1);
+ *   send_rows[...]       the rows this rank sends, as indices in its source
+ *                        local order, grouped by destination rank 0..world-1
+ *                        and, inside a group, in the destination's local
+ *                        order (sum over d of C[rank][d] entries);
+ *   recv_pos[...]        for the rows this rank receives (segments from
+ *                        ranks 0..world-1 concatenated), the position of
+ *                        each in its destination local order (sum over r of
+ *                        C[r][rank] entries); argsort of it, or a scatter by
+ *                        it, gives the local order.
+ * Any output pointer may be NULL. */
+int wp_plan_exchange(const wp_plan* plan, int src_layout, int dst_layout, int world,
+                     int rank, int64_t* counts, int* exchange_required,
+                     int32_t* send_rows, int32_t* recv_pos);
+
 /* --------------------------------------------------------------- permute --
  * wp_permute -- §Motivation/§Plan A at SP=1: the layout switch as a local row
  * permutation.  For every destination row q of dst_layout:
@@ -165,6 +197,22 @@ int wp_window_attn(const wp_plan* plan, int layout, int heads, int head_dim,
                    void* o_vid, int64_t o_vid_row_stride_B, void* o_txt,
                    void* workspace, size_t ws_bytes, float softmax_scale,
                    void* stream);
+
+/* wp_window_attn_to -- wp_window_attn with the video output written in
+ * layout `out_layout` instead of canonical order: video row r of the input
+ * layout lands at the row of `out_layout` that holds the same canonical
+ * token.  With out_layout = the next layer's layout this fuses the
+ * re-layout of §Motivation/§Plan A into the attention epilogue; the result
+ * is bit-identical to wp_window_attn followed by wp_permute(CANONICAL ->
+ * out_layout).  out_layout == layout keeps the input order.  o_txt and all
+ * other arguments as wp_window_attn; WP_EINVAL for a bad out_layout. */
+int wp_window_attn_to(const wp_plan* plan, int layout, int out_layout, int heads,
+                      int head_dim, int L, int dtype, const void* q,
+                      const void* k, const void* v, int64_t vid_row_stride_B,
+                      const void* qt, const void* kt, const void* vt,
+                      int64_t txt_row_stride_B, void* o_vid,
+                      int64_t o_vid_row_stride_B, void* o_txt, void* workspace,
+                      size_t ws_bytes, float softmax_scale, void* stream);
 
 /* wp_window_attn_static -- wp_window_attn for callers that cannot allocate
  * device memory when they run attention (a runtime that owns a fixed memory

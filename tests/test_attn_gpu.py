@@ -152,3 +152,27 @@ def test_bad_alignment_rejected(vds):
         vds.window_attn(plan, op.REGULAR, x["q"], x["k"], x["v"], x["qt"], x["kt"], x["vt"], o, t, ws)
     assert e.value.code == 2
     plan.close()
+
+
+@pytest.mark.parametrize("dtype,hd", [(torch.bfloat16, 128), (torch.float32, 64)])
+def test_output_in_another_layout_is_attention_then_permute(vds, dtype, hd):
+    """Writing the video output straight into layout b equals writing it in
+    canonical order and re-laying it out canonical -> b, bit for bit."""
+    from video_dit_shifted_gb300 import synth
+    grid, heads, L = (3, 30, 40, 2, 3, 3), 2, 20
+    plan = vds.Plan(*grid, device="cuda")
+    code = vds.BF16 if dtype == torch.bfloat16 else vds.FP32
+    for layout in (op.REGULAR, op.SHIFTED):
+        x = synth.attention_inputs(plan.N, L, heads, hd, dtype, "cuda", base_seed=3 + layout)
+        ws = vds.make_workspace(plan, layout, heads, hd, L, code, "cuda")
+        t = torch.empty((L, heads, hd), dtype=dtype, device="cuda")
+        canon = torch.empty((plan.N, heads, hd), dtype=dtype, device="cuda")
+        vds.window_attn(plan, layout, x["q"], x["k"], x["v"], x["qt"], x["kt"], x["vt"], canon, t, ws)
+        for out in (op.REGULAR, op.SHIFTED, op.CANONICAL):
+            o = torch.full_like(canon, float("nan"))
+            vds.window_attn(plan, layout, x["q"], x["k"], x["v"], x["qt"], x["kt"], x["vt"], o, t, ws,
+                            out_layout=out)
+            want = torch.empty_like(canon)
+            vds.permute(plan, canon.view(plan.N, -1), want.view(plan.N, -1), op.CANONICAL, out)
+            assert torch.equal(o, want), (layout, out)
+    plan.close()

@@ -114,7 +114,8 @@ __global__ void __launch_bounds__(kF32Rows * kF32Tpr) attn_f32_kernel(F32Params 
   }
   if (!live) return;
   const float inv = 1.f / l;
-  float* out = r < n_w ? p.o_vid + static_cast<int64_t>(p.ids[a + r]) * p.o_stride + h * HD
+  const int64_t orow = p.ids ? static_cast<int64_t>(p.ids[a + r]) : static_cast<int64_t>(a + r);
+  float* out = r < n_w ? p.o_vid + orow * p.o_stride + h * HD
                        : p.partial + ((static_cast<int64_t>(w) * p.L + (r - n_w)) * p.heads + h) * HD;
 #pragma unroll
   for (int i = 0; i < DPT; ++i) out[i * kF32Tpr + part] = acc[i] * inv;
@@ -216,13 +217,15 @@ extern "C" int wp_attn_workspace_bytes(const wp_plan* plan, int layout, int head
   return ok();
 }
 
-extern "C" int wp_window_attn(const wp_plan* plan, int layout, int heads, int head_dim, int L,
-                              int dtype, const void* q, const void* k, const void* v,
-                              int64_t vid_row_stride_B, const void* qt, const void* kt,
-                              const void* vt, int64_t txt_row_stride_B, void* o_vid,
-                              int64_t o_vid_row_stride_B, void* o_txt, void* workspace,
-                              size_t ws_bytes, float softmax_scale, void* stream) {
+namespace {
+
+int window_attn_impl(const wp_plan* plan, int layout, int out_layout, int heads, int head_dim, int L,
+                     int dtype, const void* q, const void* k, const void* v, int64_t vid_row_stride_B,
+                     const void* qt, const void* kt, const void* vt, int64_t txt_row_stride_B,
+                     void* o_vid, int64_t o_vid_row_stride_B, void* o_txt, void* workspace,
+                     size_t ws_bytes, float softmax_scale, void* stream) {
   if (int rc = check_shape(plan, layout, heads, head_dim, L, dtype)) return rc;
+  if (out_layout < 0 || out_layout >= kNumLayouts) return fail(WP_EINVAL, "bad output layout %d", out_layout);
   if (!q || !k || !v || !o_vid || !workspace) return fail(WP_EINVAL, "q, k, v, o_vid or workspace is NULL");
   if (L > 0 && (!qt || !kt || !vt || !o_txt)) return fail(WP_EINVAL, "text pointers are NULL with L=%d", L);
   const int64_t elem = dtype == WP_BF16 ? 2 : 4;
@@ -257,7 +260,15 @@ extern "C" int wp_window_attn(const wp_plan* plan, int layout, int heads, int he
   c.nwin = LT.nwin;
   c.max_tokens = LT.max_tokens;
   c.win_off = dev_ptr<int32_t>(plan, plan->dlay[layout].win_off);
-  c.ids = dev_ptr<int32_t>(plan, plan->dlay[layout].ids);
+  // Row of the output layout for each row of the input layout:
+  // canonical -> ids; the same layout -> identity (no table); another window
+  // layout b -> pos_b[ids_layout[q]], which is the fused table perm[b -> layout].
+  if (out_layout == WP_CANONICAL)
+    c.ids = dev_ptr<int32_t>(plan, plan->dlay[layout].ids);
+  else if (out_layout == layout)
+    c.ids = nullptr;
+  else
+    c.ids = dev_ptr<int32_t>(plan, plan->perm_off[out_layout][layout]);
   c.pair_off[0] = dev_ptr<int32_t>(plan, plan->dlay[layout].pair_off[0]);
   c.pair_off[1] = dev_ptr<int32_t>(plan, plan->dlay[layout].pair_off[1]);
   c.text_tiles = (L + kTileM - 1) / kTileM;
@@ -273,6 +284,30 @@ extern "C" int wp_window_attn(const wp_plan* plan, int layout, int heads, int he
   if (L > 0)
     if ((rc = launch_text_mean(c))) return rc;
   return ok();
+}
+
+}  // namespace
+
+extern "C" int wp_window_attn(const wp_plan* plan, int layout, int heads, int head_dim, int L,
+                              int dtype, const void* q, const void* k, const void* v,
+                              int64_t vid_row_stride_B, const void* qt, const void* kt,
+                              const void* vt, int64_t txt_row_stride_B, void* o_vid,
+                              int64_t o_vid_row_stride_B, void* o_txt, void* workspace,
+                              size_t ws_bytes, float softmax_scale, void* stream) {
+  return window_attn_impl(plan, layout, WP_CANONICAL, heads, head_dim, L, dtype, q, k, v, vid_row_stride_B,
+                          qt, kt, vt, txt_row_stride_B, o_vid, o_vid_row_stride_B, o_txt, workspace,
+                          ws_bytes, softmax_scale, stream);
+}
+
+extern "C" int wp_window_attn_to(const wp_plan* plan, int layout, int out_layout, int heads, int head_dim,
+                                 int L, int dtype, const void* q, const void* k, const void* v,
+                                 int64_t vid_row_stride_B, const void* qt, const void* kt,
+                                 const void* vt, int64_t txt_row_stride_B, void* o_vid,
+                                 int64_t o_vid_row_stride_B, void* o_txt, void* workspace,
+                                 size_t ws_bytes, float softmax_scale, void* stream) {
+  return window_attn_impl(plan, layout, out_layout, heads, head_dim, L, dtype, q, k, v, vid_row_stride_B,
+                          qt, kt, vt, txt_row_stride_B, o_vid, o_vid_row_stride_B, o_txt, workspace,
+                          ws_bytes, softmax_scale, stream);
 }
 
 extern "C" int wp_read_status(const void* workspace, int* device_status, void* stream) {

@@ -34,7 +34,7 @@ struct AttnCall {
   int64_t N;
   int nwin, max_tokens;
   const int32_t* win_off;      // device
-  const int32_t* ids;          // device
+  const int32_t* ids;          // device: output row of each input row (NULL: same row)
   const int32_t* pair_off[2];  // device
   int total_pairs;             // query-tile pairs over all windows (tile kTileM)
   int text_tiles;              // ceil(L / kTileM)

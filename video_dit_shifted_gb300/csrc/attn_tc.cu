@@ -81,7 +81,7 @@ static_assert(sizeof(Barriers) <= 256, "barrier block");
 
 struct TcParams {
   const int32_t* win_off;
-  const int32_t* ids;
+  const int32_t* ids;       // output row of each input row (NULL: the same row)
   const int32_t* pair_off;  // pair_off[text_tiles & 1]
   int pair_add;             // text_tiles >> 1
   int nwin, L, heads, text_tiles, total_pairs;
@@ -607,7 +607,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (t < x.vt) {
         const int tok = t * kBM + r;
         if (tok < x.n_w) {
-          __nv_bfloat16* dst = p.o_vid + static_cast<int64_t>(__ldg(p.ids + x.a + tok)) * p.o_stride + x.h * HD;
+          const int64_t orow = p.ids ? static_cast<int64_t>(__ldg(p.ids + x.a + tok)) : static_cast<int64_t>(x.a + tok);
+          __nv_bfloat16* dst = p.o_vid + orow * p.o_stride + x.h * HD;
           uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
           for (int q4 = 0; q4 < HD / 8; ++q4) {

@@ -291,3 +291,124 @@ int wp_plan_upload(wp_plan* plan, void* dev_buf, size_t bytes, void* stream) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------
+// Window -> rank assignment and the Plan A exchange tables, for running the
+// path on several devices ("Window-Aligned Sequence Parallelism (SeedVR2)",
+// §Planner and §Plan A redistribution).  Host only.
+namespace {
+
+// LPT: windows by (-token count, window id); each goes to the rank with the
+// smallest (assigned tokens, rank id).
+void lpt_assign(const LayoutTables& L, int world, std::vector<int32_t>& win_rank,
+                std::vector<int64_t>& load) {
+  std::vector<int32_t> order(L.nwin);
+  for (int w = 0; w < L.nwin; ++w) order[w] = w;
+  auto size = [&](int w) { return L.win_off[w + 1] - L.win_off[w]; };
+  std::sort(order.begin(), order.end(), [&](int a, int b) {
+    return size(a) != size(b) ? size(a) > size(b) : a < b;
+  });
+  win_rank.assign(L.nwin, 0);
+  load.assign(world, 0);
+  for (int w : order) {
+    int best = 0;
+    for (int r = 1; r < world; ++r)
+      if (load[r] < load[best]) best = r;  // ties keep the lower rank id
+    win_rank[w] = best;
+    load[best] += size(w);
+  }
+}
+
+// Rank-local order: a rank lists its windows in ascending window id, tokens
+// in layout order inside each.  For every layout row: owning rank and index
+// in that rank's local order.
+void local_rows(const LayoutTables& L, const std::vector<int32_t>& win_rank, int world,
+                std::vector<int32_t>& rank_of_row, std::vector<int32_t>& local_of_row) {
+  const int64_t N = L.win_off[L.nwin];
+  rank_of_row.assign(N, 0);
+  local_of_row.assign(N, 0);
+  std::vector<int64_t> next(world, 0);
+  for (int w = 0; w < L.nwin; ++w) {
+    const int r = win_rank[w];
+    for (int q = L.win_off[w]; q < L.win_off[w + 1]; ++q) {
+      rank_of_row[q] = r;
+      local_of_row[q] = static_cast<int32_t>(next[r]++);
+    }
+  }
+}
+
+}  // namespace
+
+extern "C" int wp_plan_assign(const wp_plan* plan, int layout, int world, int32_t* win_rank,
+                              int64_t* rank_tokens) {
+  if (!plan) return fail(WP_EINVAL, "plan is NULL");
+  if (!valid_layout(layout)) return fail(WP_EINVAL, "bad layout %d", layout);
+  if (world < 1) return fail(WP_EINVAL, "world=%d < 1", world);
+  std::vector<int32_t> wr;
+  std::vector<int64_t> load;
+  lpt_assign(plan->lay[layout], world, wr, load);
+  if (win_rank) std::memcpy(win_rank, wr.data(), wr.size() * sizeof(int32_t));
+  if (rank_tokens) std::memcpy(rank_tokens, load.data(), load.size() * sizeof(int64_t));
+  return ok();
+}
+
+extern "C" int wp_plan_exchange(const wp_plan* plan, int src_layout, int dst_layout, int world, int rank,
+                                int64_t* counts, int* exchange_required, int32_t* send_rows,
+                                int32_t* recv_pos) {
+  if (!plan) return fail(WP_EINVAL, "plan is NULL");
+  if (!valid_layout(src_layout) || !valid_layout(dst_layout))
+    return fail(WP_EINVAL, "bad layout pair (%d -> %d)", src_layout, dst_layout);
+  if (world < 1 || rank < 0 || rank >= world) return fail(WP_EINVAL, "world=%d rank=%d", world, rank);
+  const LayoutTables& S = plan->lay[src_layout];
+  const LayoutTables& D = plan->lay[dst_layout];
+  std::vector<int32_t> ws, wd, srank, slocal, drank, dlocal;
+  std::vector<int64_t> ls, ld;
+  lpt_assign(S, world, ws, ls);
+  lpt_assign(D, world, wd, ld);
+  local_rows(S, ws, world, srank, slocal);
+  local_rows(D, wd, world, drank, dlocal);
+  // C[r][d]: rows rank d needs from rank r (same canonical token).
+  std::vector<int64_t> C(static_cast<size_t>(world) * world, 0);
+  for (int64_t q = 0; q < plan->N; ++q) {
+    const int32_t c = D.ids[q];
+    const int32_t p = S.pos[c];
+    C[static_cast<size_t>(srank[p]) * world + drank[q]]++;
+  }
+  if (counts) std::memcpy(counts, C.data(), C.size() * sizeof(int64_t));
+  if (exchange_required) {
+    int any = 0;
+    for (int r = 0; r < world; ++r)
+      for (int d = 0; d < world; ++d)
+        if (r != d && C[static_cast<size_t>(r) * world + d]) any = 1;
+    *exchange_required = any;
+  }
+  // Destination-local order of every rank's rows: walk the destination layout
+  // window by window, which visits each destination rank's rows in its local
+  // order.
+  if (send_rows || recv_pos) {
+    std::vector<std::vector<int32_t>> dst_rows(world);  // dst layout rows of each rank, local order
+    for (int w = 0; w < D.nwin; ++w)
+      for (int q = D.win_off[w]; q < D.win_off[w + 1]; ++q) dst_rows[wd[w]].push_back(q);
+    if (send_rows) {
+      // For each destination d in rank order: the rows this rank holds that d
+      // needs, as this rank's local indices, in d's local order.
+      int64_t k = 0;
+      for (int d = 0; d < world; ++d)
+        for (int32_t q : dst_rows[d]) {
+          const int32_t p = S.pos[D.ids[q]];
+          if (srank[p] == rank) send_rows[k++] = slocal[p];
+        }
+    }
+    if (recv_pos) {
+      // Received segments arrive in source-rank order; each segment is in
+      // this rank's local order.  recv_pos[k] = local position of row k.
+      int64_t k = 0;
+      for (int r = 0; r < world; ++r)
+        for (int32_t q : dst_rows[rank]) {
+          const int32_t p = S.pos[D.ids[q]];
+          if (srank[p] == r) recv_pos[k++] = dlocal[q];
+        }
+    }
+  }
+  return ok();
+}

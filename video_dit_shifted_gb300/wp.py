@@ -28,6 +28,9 @@ SIGNATURES = {
     "wp_plan_info": (_c_int, [_vp, _c_int, ctypes.POINTER(_c_i64)] + [ctypes.POINTER(_c_int)] * 5),
     "wp_plan_host_tables": (_c_int, [_vp, _c_int, _pi32, _pi32, _pi32]),
     "wp_plan_device_bytes": (_c_int, [_vp, ctypes.POINTER(_c_sz)]),
+    "wp_plan_assign": (_c_int, [_vp, _c_int, _c_int, _pi32, ctypes.POINTER(_c_i64)]),
+    "wp_plan_exchange": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, ctypes.POINTER(_c_i64),
+                                  ctypes.POINTER(_c_int), _pi32, _pi32]),
     "wp_plan_upload": (_c_int, [_vp, _vp, _c_sz, _vp]),
     "wp_permute": (_c_int, [_vp, _c_int, _c_int, _vp, _c_i64, _vp, _c_i64, _c_i64, _vp]),
     "wp_attn_workspace_bytes": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int,
@@ -35,6 +38,9 @@ SIGNATURES = {
     "wp_window_attn": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int,
                                 _vp, _vp, _vp, _c_i64, _vp, _vp, _vp, _c_i64,
                                 _vp, _c_i64, _vp, _vp, _c_sz, ctypes.c_float, _vp]),
+    "wp_window_attn_to": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                   _vp, _vp, _vp, _c_i64, _vp, _vp, _vp, _c_i64,
+                                   _vp, _c_i64, _vp, _vp, _c_sz, ctypes.c_float, _vp]),
     "wp_window_attn_static": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int,
                                        _vp, _vp, _vp, _c_i64, _vp, _vp, _vp, _c_i64,
                                        _vp, _c_i64, _vp, ctypes.c_float, _vp]),
@@ -115,6 +121,29 @@ class Plan:
         _check("wp_plan_host_tables", lib().wp_plan_host_tables(self.handle, layout, p(off), p(ids), p(boxes)))
         return off, ids, boxes.reshape(nwin, 6)
 
+    def assign(self, layout, world):
+        """(win_rank[nwin], rank_tokens[world]) of the LPT window -> rank plan."""
+        nwin = self.info(layout)["nwin"]
+        wr = np.zeros(nwin, np.int32)
+        load = np.zeros(world, np.int64)
+        _check("wp_plan_assign", lib().wp_plan_assign(self.handle, layout, world, wr.ctypes.data_as(_pi32),
+                                                      load.ctypes.data_as(ctypes.POINTER(_c_i64))))
+        return wr, load
+
+    def exchange(self, src_layout, dst_layout, world, rank):
+        """(counts[world, world], exchange_required, send_rows, recv_pos) of Plan A."""
+        C = np.zeros((world, world), np.int64)
+        req = _c_int()
+        _check("wp_plan_exchange", lib().wp_plan_exchange(
+            self.handle, src_layout, dst_layout, world, rank, C.ctypes.data_as(ctypes.POINTER(_c_i64)),
+            ctypes.byref(req), None, None))
+        send = np.zeros(int(C[rank].sum()), np.int32)
+        recv = np.zeros(int(C[:, rank].sum()), np.int32)
+        _check("wp_plan_exchange", lib().wp_plan_exchange(
+            self.handle, src_layout, dst_layout, world, rank, None, None,
+            send.ctypes.data_as(_pi32), recv.ctypes.data_as(_pi32)))
+        return C, bool(req.value), send, recv
+
     def device_bytes(self):
         b = _c_sz()
         _check("wp_plan_device_bytes", lib().wp_plan_device_bytes(self.handle, ctypes.byref(b)))
@@ -176,20 +205,22 @@ def make_workspace(plan, layout, heads, head_dim, L, dtype_code, device):
                        dtype=torch.uint8, device=device)
 
 
-def window_attn(plan, layout, q, k, v, qt, kt, vt, o_vid, o_txt, workspace, scale=0.0, stream=None):
-    """One layer of window attention (see wp_window_attn in include/wp.h).
+def window_attn(plan, layout, q, k, v, qt, kt, vt, o_vid, o_txt, workspace, scale=0.0, stream=None,
+                out_layout=CANONICAL):
+    """One layer of window attention (wp_window_attn_to in include/wp.h).
 
     q, k, v: [N, heads, hd] views in `layout` order sharing one row stride;
     qt, kt, vt: [L, heads, hd] sharing one row stride; o_vid [N, heads, hd]
-    (canonical order); o_txt [L, heads, hd] contiguous."""
+    in `out_layout` order (canonical by default); o_txt [L, heads, hd]
+    contiguous."""
     N, heads, hd = q.shape
     L = qt.shape[0] if qt is not None else 0
     es = q.element_size()
     if not (k.stride(0) == v.stride(0) == q.stride(0)):
         raise ValueError("q, k, v must share one row stride")
     txt_stride = qt.stride(0) * es if L else 0
-    _check("wp_window_attn", lib().wp_window_attn(
-        plan.handle, layout, heads, hd, L, _dtype_code(q),
+    _check("wp_window_attn_to", lib().wp_window_attn_to(
+        plan.handle, layout, out_layout, heads, hd, L, _dtype_code(q),
         _ptr(q), _ptr(k), _ptr(v), q.stride(0) * es,
         _ptr(qt if L else None), _ptr(kt if L else None), _ptr(vt if L else None), txt_stride,
         _ptr(o_vid), o_vid.stride(0) * es, _ptr(o_txt if L else None),
