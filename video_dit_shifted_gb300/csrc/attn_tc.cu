@@ -7,21 +7,30 @@
 // results are scattered to their canonical rows, text results T_w are written
 // in fp32 for the ordered mean in attn.cu.
 //
-// Design (one CTA per pair of 128-row query tiles of one (window, head)):
-//   warp 0      TMA producer: Q tiles once, then K and V tiles of the segment
-//               (video tiles of the window, then text tiles) into a 2-stage
-//               ring each, 128-byte swizzled, 64 columns per box;
-//   warp 1      MMA issuer (one thread): S_i = Q_i K_j^T (SS form) into TMEM,
-//               O_i += P_i V_j with P_i read from TMEM (TS form);
-//   warp 2      TMEM allocator (512 columns: S0, S1, O0, O1);
-//   warps 4-7   softmax for query tile 0, warps 8-11 for query tile 1: one
-//               thread per query row (TMEM lane), online softmax in the log2
-//               domain, P written back over S as packed bf16, O rescaled in
-//               TMEM only when the running max grows by more than 2^8 (the
-//               final O / l is exact either way), then the epilogue.
-// The two query tiles share every K/V tile, and the MMA order
+// Design.  Work items are pairs of 128-row query tiles of one (window, head);
+// a persistent grid of one CTA per SM walks them round-robin (items of one
+// (window, head) are adjacent, so CTAs busy at the same time share K/V tiles
+// through L2).  Roles inside a CTA (320 threads):
+//   warps 0-3   softmax + epilogue for query tile 0, warps 4-7 for tile 1:
+//               one thread per query row (TMEM lane); one 128-column TMEM
+//               load of S per tile, row max, 2^x in the log2 domain, P
+//               written back over S as packed bf16; O is rescaled in TMEM
+//               only when a row max grows by more than 2^8 (the final O / l
+//               is exact either way); the epilogue scatters video rows to
+//               their output rows and writes text rows as fp32 T_w;
+//   warp 8      TMA producer: both Q tiles of an item, then the item's K and
+//               V tiles (video tiles of the window, then text tiles) into a
+//               2-stage ring each, 128-byte swizzled, 64 columns per box;
+//               the next item's loads start as soon as buffers free up;
+//   warp 9      TMEM allocator (512 columns: S0, S1, O0, O1) and MMA issuer
+//               (one thread): S_i = Q_i K_j^T (both operands in shared
+//               memory) and O_i += P_i V_j (P from TMEM, V MN-major).
+// The two query tiles share every K/V tile, and the issue order
 // S0(j) S1(j) PV0(j) S0(j+1) PV1(j) S1(j+1) ... lets one tile's softmax run
-// while the tensor core works on the other.
+// while the tensor core works on the other.  The tensor pipe queues only
+// about two MMAs, so the issue loop is kept free of anything slow: the wait
+// fast path is inlined, descriptors advance by constants, and the tile index
+// is a compile-time constant.
 //
 // Masking: a segment is ragged, so the last video K/V tile of a window may
 // run into the next window's rows (or past N, where TMA fills zeros).  Those
