@@ -449,6 +449,23 @@ def run_ours(args):
     e2e = {"value": world * step_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
            "steps": args.e2e_steps}
+    # Window-local RoPE of q and k (a separate in-place pass, not part of the
+    # step): HBM-bound, 2 tensors x (read + write) x rows x heads x 128 x 2 B.
+    b, t = wl.qkv[vds.REGULAR], wl.txt
+    rope_bytes = 2 * 2 * (wl.N + wl.w["L"]) * wl.w["heads"] * wl.w["hd"] * 2
+    for _ in range(2):
+        vds.rope(wl.plan, vds.REGULAR, b[:, 0], b[:, 1], t[:, 0], t[:, 1])
+    r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    r0.record()
+    for _ in range(10):
+        vds.rope(wl.plan, vds.REGULAR, b[:, 0], b[:, 1], t[:, 0], t[:, 1])
+    r1.record()
+    torch.cuda.synchronize()
+    rope_ms = r0.elapsed_time(r1) / 10
+    peaks_r, _ = load_peaks()
+    rope = {"bound": "hbm", "achieved": rope_bytes / (rope_ms * 1e-3) / 1e9, "peak": peaks_r["hbm_gbs"],
+            "unit": "GB/s", "frac": rope_bytes / (rope_ms * 1e-3) / 1e9 / peaks_r["hbm_gbs"], "ms": rope_ms,
+            "bytes_per_launch": rope_bytes, "kernel": "rope_kernel (regular layout, q and k in place)"}
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tf, pairs, fl, secs = oracle_sample(args.workload, args.cpu_budget_s)
@@ -464,7 +481,8 @@ def run_ours(args):
                                  % (wl.qkv[vds.REGULAR].numel() * 2 / 1e9, wl.hidden.numel() * 2 / 1e9),
                            "parallelism": "replicas" if world > 1 else "single GPU"},
                 "attn_tflops": attn_tflops, "relayout_gbs": relayout_gbs,
-                "roofline": roofline, "roofline_relayout": relayout, "cpu_baseline": cpu, "e2e": e2e,
+                "roofline": roofline, "roofline_relayout": relayout, "roofline_rope": rope,
+                "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": wl.launches_per_step * args.steps, "clocks": clk}
         print(json.dumps(line), flush=True)
     if pg is not None:

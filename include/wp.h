@@ -160,6 +160,24 @@ int wp_permute(const wp_plan* plan, int src_layout, int dst_layout,
                const void* src, int64_t src_stride_B, void* dst,
                int64_t dst_stride_B, int64_t row_B, void* stream);
 
+/* ------------------------------------------------------------------ rope --
+ * wp_rope -- window-local 3D rotary position embedding of q and k, in place
+ * (§Reference quirks reproduced on purpose): a video token at window-local
+ * (dt, dh, dw) of `layout` uses the axial indices (L + dt, dh, dw), every
+ * window restarting at 0; the rotary span is 3*(head_dim/3) = 126 channels,
+ * the last two pass through.  Readings where the page is silent: axis
+ * blocks t, h, w of 42 channels; channels (2i, 2i+1) of a block rotate by
+ * pos * rope_base^(-2i/42) (rope_base 10000 is the usual value); a text
+ * token at position l uses (l, l, l).
+ * q, k: [N, heads, 128] rows in `layout` order (shared row stride); qt, kt:
+ * [L, heads, 128] (shared stride; may be NULL iff L == 0).  dtype WP_BF16
+ * (rotated in fp32, rounded to nearest even) or WP_FP32.
+ * WP_EUNSUPPORTED: head_dim != 128, misaligned pointers or strides;
+ * WP_EINVAL: bad layout/dtype, NULL pointers, rope_base <= 1. */
+int wp_rope(const wp_plan* plan, int layout, int heads, int head_dim, int L,
+            int dtype, void* q, void* k, int64_t vid_row_stride_B, void* qt,
+            void* kt, int64_t txt_row_stride_B, float rope_base, void* stream);
+
 /* ------------------------------------------------------------- attention --
  * wp_attn_workspace_bytes -- device workspace wp_window_attn needs: a
  * 256-byte status block plus the per-window text outputs

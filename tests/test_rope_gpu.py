@@ -1,0 +1,91 @@
+"""wp_rope (window-local 3D RoPE, in place) against the oracle (gpu)."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as oa
+from oracle import plan as op
+from oracle import rope as orp
+
+pytestmark = pytest.mark.gpu
+
+TOL = {torch.bfloat16: 2e-2, torch.float32: 5e-4}
+
+
+@pytest.fixture(scope="module")
+def vds():
+    import __graft_entry__
+    __graft_entry__.build()
+    import video_dit_shifted_gb300 as m
+    return m
+
+
+def _np(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("L", [0, 5])
+def test_rope_matches_oracle(vds, dtype, L):
+    from video_dit_shifted_gb300 import synth
+    grid, heads = (3, 30, 40, 2, 3, 3), 3
+    plan = vds.Plan(*grid, device="cuda")
+    for layout in (op.REGULAR, op.SHIFTED, op.CANONICAL):
+        x = synth.attention_inputs(plan.N, max(L, 1), heads, 128, dtype, "cuda", base_seed=layout)
+        qt, kt = (x["qt"], x["kt"]) if L else (None, None)
+        before = {n: _np(x[n]) for n in ("q", "k", "qt", "kt")}
+        vds.rope(plan, layout, x["q"], x["k"], qt, kt)
+        torch.cuda.synchronize()
+        pv, pt = orp.positions(*grid, layout, L)
+        for n, pos in (("q", pv), ("k", pv)) + ((("qt", pt), ("kt", pt)) if L else ()):
+            want = orp.rope(before[n], pos)
+            assert np.abs(_np(x[n]) - want).max() <= TOL[dtype], (layout, n)
+    plan.close()
+
+
+def test_rope_then_attention(vds):
+    """RoPE in the layer's layout followed by window attention equals the
+    oracle's rotated attention."""
+    from video_dit_shifted_gb300 import synth
+    grid, heads, L = (2, 45, 80, 1, 3, 3), 2, 16
+    plan = vds.Plan(*grid, device="cuda")
+    for layout in (op.REGULAR, op.SHIFTED):
+        x = synth.attention_inputs(plan.N, L, heads, 128, torch.bfloat16, "cuda", base_seed=5 * layout)
+        raw = {n: _np(x[n]) for n in ("q", "k", "v", "qt", "kt", "vt")}
+        vds.rope(plan, layout, x["q"], x["k"], x["qt"], x["kt"])
+        o = torch.empty((plan.N, heads, 128), dtype=torch.bfloat16, device="cuda")
+        t = torch.empty((L, heads, 128), dtype=torch.bfloat16, device="cuda")
+        ws = vds.make_workspace(plan, layout, heads, 128, L, vds.BF16, "cuda")
+        vds.window_attn(plan, layout, x["q"], x["k"], x["v"], x["qt"], x["kt"], x["vt"], o, t, ws)
+        pv, pt = orp.positions(*grid, layout, L)
+        off, ids = op.layout_tables(*grid, layout)
+        ref_o, ref_t = oa.window_attention(orp.rope(raw["q"], pv), orp.rope(raw["k"], pv), raw["v"],
+                                           orp.rope(raw["qt"], pt), orp.rope(raw["kt"], pt), raw["vt"], off, ids)
+        assert np.abs(_np(o) - ref_o).max() <= 2e-2
+        assert np.abs(_np(t) - oa.text_mean(ref_t)).max() <= 2e-2
+    plan.close()
+
+
+def test_rope_1080p_sampled_rows(vds):
+    from video_dit_shifted_gb300 import synth
+    grid, heads, L = (21, 68, 120, 4, 3, 3), 24, 256
+    plan = vds.Plan(*grid, device="cuda")
+    x = synth.attention_inputs(plan.N, L, heads, 128, torch.bfloat16, "cuda")
+    rows = np.random.default_rng(0).choice(plan.N, 2048, replace=False)
+    idx = torch.from_numpy(rows).cuda()
+    before_q, before_qt = _np(x["q"][idx]), _np(x["qt"])
+    vds.rope(plan, op.SHIFTED, x["q"], x["k"], x["qt"], x["kt"])
+    torch.cuda.synchronize()
+    pv, pt = orp.positions(*grid, op.SHIFTED, L)
+    assert np.abs(_np(x["q"][idx]) - orp.rope(before_q, pv[rows])).max() <= 2e-2
+    assert np.abs(_np(x["qt"]) - orp.rope(before_qt, pt)).max() <= 2e-2
+    plan.close()
+
+
+def test_rope_rejects_head_dim_64(vds):
+    plan = vds.Plan(2, 45, 80, 1, 3, 3, device="cuda")
+    q = torch.zeros((plan.N, 2, 64), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(vds.wp.WpError) as e:
+        vds.rope(plan, op.REGULAR, q, q.clone(), None, None)
+    assert e.value.code == 2
+    plan.close()

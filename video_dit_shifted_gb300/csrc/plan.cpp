@@ -129,6 +129,7 @@ size_t layout_device(wp_plan* p) {
     p->dlay[l].ids = take(p->N);
     p->dlay[l].pair_off[0] = take(L.nwin + 1);
     p->dlay[l].pair_off[1] = take(L.nwin + 1);
+    p->dlay[l].boxes = take(static_cast<size_t>(L.nwin) * 6);
   }
   for (int a = 0; a < kNumLayouts; ++a)
     for (int b = 0; b < kNumLayouts; ++b)
@@ -270,6 +271,7 @@ int wp_plan_upload(wp_plan* plan, void* dev_buf, size_t bytes, void* stream) {
     put(plan->dlay[l].ids, L.ids);
     put(plan->dlay[l].pair_off[0], L.pair_off[0]);
     put(plan->dlay[l].pair_off[1], L.pair_off[1]);
+    put(plan->dlay[l].boxes, L.boxes);
   }
   for (int a = 0; a < kNumLayouts; ++a)
     for (int b = 0; b < kNumLayouts; ++b) {

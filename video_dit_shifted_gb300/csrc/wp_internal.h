@@ -38,7 +38,7 @@ struct LayoutTables {
 
 // Offsets (bytes) of each table inside the caller's device buffer.
 struct DeviceLayout {
-  size_t win_off = 0, ids = 0, pair_off[2] = {0, 0};
+  size_t win_off = 0, ids = 0, pair_off[2] = {0, 0}, boxes = 0;
 };
 
 }  // namespace wp

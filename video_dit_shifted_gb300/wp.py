@@ -33,6 +33,8 @@ SIGNATURES = {
                                   ctypes.POINTER(_c_int), _pi32, _pi32]),
     "wp_plan_upload": (_c_int, [_vp, _vp, _c_sz, _vp]),
     "wp_permute": (_c_int, [_vp, _c_int, _c_int, _vp, _c_i64, _vp, _c_i64, _c_i64, _vp]),
+    "wp_rope": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _c_i64, _vp, _vp, _c_i64,
+                         ctypes.c_float, _vp]),
     "wp_attn_workspace_bytes": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int,
                                          ctypes.POINTER(_c_sz)]),
     "wp_window_attn": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int,
@@ -183,6 +185,19 @@ def permute(plan, src, dst, src_layout, dst_layout, stream=None):
                                           dst.stride(0) * dst.element_size(), row_B,
                                           _stream_ptr(stream)))
     return dst
+
+
+def rope(plan, layout, q, k, qt, kt, base=10000.0, stream=None):
+    """In-place window-local 3D RoPE of q, k [N, heads, 128] (layout order)
+    and qt, kt [L, heads, 128] (see wp_rope in include/wp.h)."""
+    N, heads, hd = q.shape
+    L = qt.shape[0] if qt is not None else 0
+    es = q.element_size()
+    if k.stride(0) != q.stride(0) or (L and kt.stride(0) != qt.stride(0)):
+        raise ValueError("q and k (and qt and kt) must share one row stride")
+    _check("wp_rope", lib().wp_rope(plan.handle, layout, heads, hd, L, _dtype_code(q), _ptr(q), _ptr(k),
+                                    q.stride(0) * es, _ptr(qt if L else None), _ptr(kt if L else None),
+                                    qt.stride(0) * es if L else 0, float(base), _stream_ptr(stream)))
 
 
 def _dtype_code(t):
