@@ -176,3 +176,43 @@ def test_output_in_another_layout_is_attention_then_permute(vds, dtype, hd):
             vds.permute(plan, canon.view(plan.N, -1), want.view(plan.N, -1), op.CANONICAL, out)
             assert torch.equal(o, want), (layout, out)
     plan.close()
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_more_than_30_frames(vds, dtype):
+    """T > 30: the temporal window is capped at ceil(30/nt), so the regular
+    layout has more t windows than nt."""
+    grid = (33, 6, 8, 2, 1, 1)
+    assert op.window_size(*grid)[0] == 15
+    _check_full(vds, grid, 2, 128 if dtype == torch.bfloat16 else 64, 9, dtype)
+
+
+def test_long_odd_text(vds):
+    """L = 520: five text tiles, the last one ragged; three heads."""
+    _check_full(vds, (2, 20, 30, 1, 2, 2), 3, 128, 520, torch.bfloat16)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_separate_tensors_and_strided_output(vds, dtype):
+    """q, k, v as separate contiguous tensors; o_vid rows inside a wider
+    buffer (row stride larger than heads * head_dim); guard columns stay
+    untouched."""
+    from video_dit_shifted_gb300 import synth
+    grid, heads, L = (3, 30, 40, 2, 3, 3), 2, 16
+    hd = 128 if dtype == torch.bfloat16 else 64
+    plan = vds.Plan(*grid, device="cuda")
+    code = vds.BF16 if dtype == torch.bfloat16 else vds.FP32
+    for layout in (op.REGULAR, op.SHIFTED):
+        x = synth.attention_inputs(plan.N, L, heads, hd, dtype, "cuda", base_seed=11, packed=False)
+        wide = torch.full((plan.N, heads + 1, hd), 7.0, dtype=dtype, device="cuda")
+        o = wide[:, :heads]                     # row stride (heads + 1) * hd
+        t = torch.empty((L, heads, hd), dtype=dtype, device="cuda")
+        ws = vds.make_workspace(plan, layout, heads, hd, L, code, "cuda")
+        vds.window_attn(plan, layout, x["q"], x["k"], x["v"], x["qt"], x["kt"], x["vt"], o, t, ws)
+        assert vds.read_status(ws) == 0
+        off, ids = op.layout_tables(*grid, layout)
+        ref_o, ref_t = oa.window_attention(*(_np(x[n]) for n in ("q", "k", "v", "qt", "kt", "vt")), off, ids)
+        assert np.abs(_np(o) - ref_o).max() <= TOL[dtype]
+        assert np.abs(_np(t) - oa.text_mean(ref_t)).max() <= TOL[dtype]
+        assert torch.all(wide[:, heads] == 7.0)
+    plan.close()
