@@ -305,10 +305,9 @@ __device__ __forceinline__ float row_exp(const uint32_t (&s)[128], int valid, fl
     acc[e & 3] = fadd2(acc[e & 3], f2_pack(p0, p1));
     pk[e] = pack_bf16(p0, p1);
   }
-  float a0, a1, b0, b1, c0, c1, d0, d1;
+  float a0, a1, b0, b1;
   f2_unpack(fadd2(acc[0], acc[1]), a0, a1);
   f2_unpack(fadd2(acc[2], acc[3]), b0, b1);
-  (void)c0; (void)c1; (void)d0; (void)d1;
   return (a0 + a1) + (b0 + b1);
 }
 
