@@ -34,44 +34,43 @@ def items_for(grid, L, heads, nblocks, b, layout=op.REGULAR):
     items=[pairs[it % len(pairs)] for it in range(len(pairs)*heads)]
     return items[b::nblocks]
 
-COUNT={'q_full':1,'q_empty':1,'k_full0':1,'k_full1':1,'v_full0':1,'v_full1':1,'k_empty0':1,'k_empty1':1,
-       'v_empty0':1,'v_empty1':1,'s_full0':1,'s_full1':1,'p_full0':1,'p_full1':1,'o_full0':1,'o_full1':1,
+COUNT={'q_full':1,'q_empty':1,'pl_full0':1,'pl_full1':1,'pl_empty0':1,'pl_empty1':1,
+       's_full0':1,'s_full1':1,'p_full0':1,'p_full1':1,'o_full0':1,'o_full1':1,
        'o_empty0':1,'o_empty1':1}
 
 def producer(items):
-    gk=gv=0; k=0
+    # payload e (global): item start -> [K(g0)]; step j -> [V(g0+j), K(g0+j+1)] (K only if
+    # the item has tile j+1).  Payload e lives in slot e&1; it may load once payload e-2
+    # is released (its tiles use the same K/V stages).
+    e=0; k=0
     for (w,nkv,nq) in items:
         if k>0: yield ('wait','q_empty',k-1)
         yield ('arrive','q_full'); k+=1
-        for j in range(nkv):
-            s=gk&1
-            if gk>=2: yield ('wait','k_empty%d'%s,(gk>>1)-1)
-            yield ('arrive','k_full%d'%s); gk+=1
-            s=gv&1
-            if gv>=2: yield ('wait','v_empty%d'%s,(gv>>1)-1)
-            yield ('arrive','v_full%d'%s); gv+=1
-
+        for p in range(nkv+1):
+            if e>=2: yield ('wait','pl_empty%d'%(e&1),(e>>1)-1)
+            yield ('arrive','pl_full%d'%(e&1))
+            e+=1
 def mma(items):
-    g=0; k=0; cs=[0,0]; co=[0,0]
+    e=0; k=0; cs=[0,0]; co=[0,0]
     for (w,nkv,nq) in items:
         yield ('wait','q_full',k)
-        yield ('wait','k_full%d'%(g&1),g>>1)
+        yield ('wait','pl_full%d'%(e&1),e>>1)          # payload [K(0)]
         for i in range(nq): yield ('commit','s_full%d'%i)
-        yield ('commit','k_empty%d'%(g&1))
         if nkv==1: yield ('commit','q_empty')
+        yield ('commit','pl_empty%d'%(e&1))            # K(0) read by the S(0) just issued
+        e+=1
         for j in range(nkv):
-            s=(g+j)&1; sn=(g+j+1)&1; more=j+1<nkv
-            yield ('wait','v_full%d'%s,(g+j)>>1)
-            if more: yield ('wait','k_full%d'%sn,(g+j+1)>>1)
+            more=j+1<nkv
+            yield ('wait','pl_full%d'%(e&1),e>>1)      # payload [V(j), K(j+1)]
             for i in range(nq):
                 yield ('wait','p_full%d'%i,cs[i]+j)
                 if j==0 and co[i]>0: yield ('wait','o_empty%d'%i,co[i]-1)
                 yield ('commit',('s_full%d' if more else 'o_full%d')%i)
-            yield ('commit','v_empty%d'%s)
-            if more: yield ('commit','k_empty%d'%sn)
+            yield ('commit','pl_empty%d'%(e&1))        # V(j) and K(j+1) read by MMAs just issued
             if j+2==nkv: yield ('commit','q_empty')
+            e+=1
         for i in range(nq): cs[i]+=nkv; co[i]+=1
-        g+=nkv; k+=1
+        k+=1
 
 def softmax(items,i):
     cs=0; co=0

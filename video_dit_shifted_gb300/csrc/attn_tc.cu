@@ -19,9 +19,10 @@
 //               is exact either way); the epilogue scatters video rows to
 //               their output rows and writes text rows as fp32 T_w;
 //   warp 8      TMA producer: both Q tiles of an item, then the item's K and
-//               V tiles (video tiles of the window, then text tiles) into a
-//               2-stage ring each, 128-byte swizzled, 64 columns per box;
-//               the next item's loads start as soon as buffers free up;
+//               V tiles (video tiles of the window, then text tiles) in
+//               per-step payloads [K_0], [V_0, K_1], [V_1, K_2], ... into two
+//               K and two V slots, 128-byte swizzled, 64 columns per box; the
+//               next item's loads start as soon as slots free up;
 //   warp 9      TMEM allocator (512 columns: S0, S1, O0, O1) and MMA issuer
 //               (one thread): S_i = Q_i K_j^T (both operands in shared
 //               memory) and O_i += P_i V_j (P from TMEM, V MN-major).
@@ -80,7 +81,7 @@ constexpr int kSmemBytes = Cfg<128>::kBar + 256 + 1024;
 
 struct Barriers {
   uint64_t q_full, q_empty;
-  uint64_t k_full[2], v_full[2], k_empty[2], v_empty[2];
+  uint64_t pl_full[2], pl_empty[2];  // K/V payload slots (see the producer)
   uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
   uint64_t mma_done;
   uint32_t tmem_base;
@@ -365,10 +366,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bq_full, 1);
     mbar_init(bq_empty, 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(bars->k_full[s]), 1);
-      mbar_init(bar(bars->v_full[s]), 1);
-      mbar_init(bar(bars->k_empty[s]), 1);
-      mbar_init(bar(bars->v_empty[s]), 1);
+      mbar_init(bar(bars->pl_full[s]), 1);
+      mbar_init(bar(bars->pl_empty[s]), 1);
       mbar_init(bar(bars->s_full[s]), 1);
       mbar_init(bar(bars->p_full[s]), 128);
       mbar_init(bar(bars->o_full[s]), 1);
@@ -397,8 +396,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kProducerWarp) {
     // ======================= TMA producer ===============================
     if (lane == 0) {
-      int gk = 0, gv = 0;  // K and V tiles issued so far (ring positions)
-      int k = 0;           // items whose Q load was issued
+      // K/V tiles travel in "payloads", one per MMA step, so that the MMA
+      // thread waits once and releases once per step: an item starts with
+      // [K_0]; step j of the item brings [V_j, K_{j+1}] (K only while the
+      // item has a next tile).  Payload e fills K slot e&1 and V slot e&1 and
+      // may load once payload e-2 is released, i.e. once the MMAs of the
+      // step that consumed it have completed.
+      int e = 0;  // payloads issued
+      int k = 0;  // items whose Q load was issued
       bool good = true;
       for (int it = blockIdx.x; it < n_items && good; it += gridDim.x) {
         const Item x = decode_item(p, it);
@@ -414,33 +419,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                         x.h * HD + hf * 64, row);
         }
         ++k;
-        for (int j = 0; j < x.nkv; ++j) {
-          const bool vid = j < x.vt;
-          const int row = vid ? x.a + j * kBN : (j - x.vt) * kBN;
-          const int s = gk & 1;
-          if (gk >= 2 && !(good = wait_phase(bar(bars->k_empty[s]), ((gk >> 1) - 1) & 1, abort_flag, p.status)))
+        auto tile_row = [&](int j) { return j < x.vt ? x.a + j * kBN : (j - x.vt) * kBN; };
+        for (int pl = 0; pl <= x.nkv; ++pl, ++e) {
+          const int slot = e & 1;
+          if (e >= 2 && !(good = wait_phase(bar(bars->pl_empty[slot]), ((e >> 1) - 1) & 1, abort_flag, p.status)))
             break;
-          mbar_expect_tx(bar(bars->k_full[s]), C::kTileBytes);
-          for (int hf = 0; hf < C::kHalves; ++hf)
-            tma_load_2d(base + C::kK + s * C::kTileBytes + hf * C::kBoxBytes, vid ? &tm_k : &tm_kt,
-                        bar(bars->k_full[s]), x.h * HD + hf * 64, row);
-          ++gk;
-          if (gv >= 2 && !(good = wait_phase(bar(bars->v_empty[s]), ((gv >> 1) - 1) & 1, abort_flag, p.status)))
-            break;
-          mbar_expect_tx(bar(bars->v_full[s]), C::kTileBytes);
-          for (int hf = 0; hf < C::kHalves; ++hf)
-            tma_load_2d(base + C::kV + s * C::kTileBytes + hf * C::kBoxBytes, vid ? &tm_v : &tm_vt,
-                        bar(bars->v_full[s]), x.h * HD + hf * 64, row);
-          ++gv;
+          const int kt = pl;      // K tile of this payload (none when pl == nkv)
+          const int vt_ = pl - 1;  // V tile of this payload (none when pl == 0)
+          const uint32_t fb = bar(bars->pl_full[slot]);
+          mbar_expect_tx(fb, ((kt < x.nkv) + (vt_ >= 0)) * C::kTileBytes);
+          if (vt_ >= 0)
+            for (int hf = 0; hf < C::kHalves; ++hf)
+              tma_load_2d(base + C::kV + slot * C::kTileBytes + hf * C::kBoxBytes, vt_ < x.vt ? &tm_v : &tm_vt,
+                          fb, x.h * HD + hf * 64, tile_row(vt_));
+          if (kt < x.nkv)
+            for (int hf = 0; hf < C::kHalves; ++hf)
+              tma_load_2d(base + C::kK + slot * C::kTileBytes + hf * C::kBoxBytes, kt < x.vt ? &tm_k : &tm_kt,
+                          fb, x.h * HD + hf * 64, tile_row(kt));
         }
       }
       if (*abort_flag) {
         // Let every copy this thread started land before the CTA exits.
         if (k > 0) drain_wait(bq_full, (k - 1) & 1);
-        for (int u = gk - 2; u < gk; ++u)
-          if (u >= 0) drain_wait(bar(bars->k_full[u & 1]), (u >> 1) & 1);
-        for (int u = gv - 2; u < gv; ++u)
-          if (u >= 0) drain_wait(bar(bars->v_full[u & 1]), (u >> 1) & 1);
+        for (int u = e - 2; u < e; ++u)
+          if (u >= 0) drain_wait(bar(bars->pl_full[u & 1]), (u >> 1) & 1);
       }
     }
   } else if (warp == kMmaWarp) {
@@ -469,7 +471,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < kBN / 16; ++kk)
           mma_ts(dO, aP + kk * 8, vd + ((kk * 2048) >> 4), kIdescPV, (!first || kk > 0) ? 1u : 0u);
       };
-      int g = 0;                  // K/V tiles consumed
       int k = 0;                  // items
       int cs0 = 0, cs1 = 0;       // tiles per softmax warpgroup (s_full / p_full phases)
       int co0 = 0, co1 = 0;       // items per softmax warpgroup (o_full / o_empty phases)
@@ -494,31 +495,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return true;
       };
+      int e = 0;  // payloads consumed (see the producer)
       for (int it = blockIdx.x; it < n_items && good; it += gridDim.x, ++k) {
         const Item x = decode_item(p, it);
+        // payload [K_0]
         if (!(good = wait_phase(bq_full, k & 1, abort_flag, p.status) &&
-                     wait_phase(bar(bars->k_full[g & 1]), (g >> 1) & 1, abort_flag, p.status)))
+                     wait_phase(bar(bars->pl_full[e & 1]), (e >> 1) & 1, abort_flag, p.status)))
           break;
         tc_fence_after();
-        issue_qk(0, g & 1);
+        issue_qk(0, e & 1);
         mma_commit(bar(bars->s_full[0]));
         if (x.nq > 1) {
-          issue_qk(1, g & 1);
+          issue_qk(1, e & 1);
           mma_commit(bar(bars->s_full[1]));
         }
-        mma_commit(bar(bars->k_empty[g & 1]));
         if (x.nkv == 1) mma_commit(bq_empty);
-        for (int j = 0; j < x.nkv; ++j) {
-          const int s = (g + j) & 1, sn = (g + j + 1) & 1;
+        mma_commit(bar(bars->pl_empty[e & 1]));
+        ++e;
+        for (int j = 0; j < x.nkv; ++j, ++e) {
+          const int s = e & 1;  // payload [V_j, K_{j+1}]
           const bool more = j + 1 < x.nkv;
-          // V_j for this step and K_{j+1} for the next: usually landed long ago.
-          if (!(good = wait_phase(bar(bars->v_full[s]), ((g + j) >> 1) & 1, abort_flag, p.status))) break;
-          if (more && !(good = wait_phase(bar(bars->k_full[sn]), ((g + j + 1) >> 1) & 1, abort_flag, p.status)))
-            break;
-          if (!(good = tile_step(std::integral_constant<int, 0>{}, j, s, sn, more, cs0, co0))) break;
-          if (x.nq > 1 && !(good = tile_step(std::integral_constant<int, 1>{}, j, s, sn, more, cs1, co1))) break;
-          mma_commit(bar(bars->v_empty[s]));
-          if (more) mma_commit(bar(bars->k_empty[sn]));
+          if (!(good = wait_phase(bar(bars->pl_full[s]), (e >> 1) & 1, abort_flag, p.status))) break;
+          if (!(good = tile_step(std::integral_constant<int, 0>{}, j, s, s, more, cs0, co0))) break;
+          if (x.nq > 1 && !(good = tile_step(std::integral_constant<int, 1>{}, j, s, s, more, cs1, co1))) break;
+          mma_commit(bar(bars->pl_empty[s]));
           if (j + 2 == x.nkv) mma_commit(bq_empty);  // the Q K^T just issued was the item's last
         }
         cs0 += x.nkv;
@@ -527,7 +527,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           cs1 += x.nkv;
           co1 += 1;
         }
-        g += x.nkv;
       }
       // All MMAs this thread issued must finish before TMEM is freed.
       mma_commit(bar(bars->mma_done));
