@@ -216,3 +216,44 @@ def test_separate_tensors_and_strided_output(vds, dtype):
         assert np.abs(_np(t) - oa.text_mean(ref_t)).max() <= TOL[dtype]
         assert torch.all(wide[:, heads] == 7.0)
     plan.close()
+
+
+def test_layer_pair_replays_in_a_cuda_graph(vds):
+    """attention (regular) -> re-layout -> attention (shifted), captured once
+    in a CUDA graph and replayed, gives the eager results bit for bit."""
+    from video_dit_shifted_gb300 import synth
+    grid, heads, hd, L = (3, 30, 40, 2, 3, 3), 2, 128, 16
+    plan = vds.Plan(*grid, device="cuda")
+    N = plan.N
+    x = synth.attention_inputs(N, L, heads, hd, torch.bfloat16, "cuda")
+    qkv_shf = torch.empty_like(x["vid_buf"])
+    outs = {l: torch.empty((N, heads, hd), dtype=torch.bfloat16, device="cuda") for l in (op.REGULAR, op.SHIFTED)}
+    txt = {l: torch.empty((L, heads, hd), dtype=torch.bfloat16, device="cuda") for l in (op.REGULAR, op.SHIFTED)}
+    ws = {l: vds.make_workspace(plan, l, heads, hd, L, vds.BF16, "cuda") for l in (op.REGULAR, op.SHIFTED)}
+
+    def layer_pair():
+        b = x["vid_buf"]
+        vds.window_attn(plan, op.REGULAR, b[:, 0], b[:, 1], b[:, 2], x["qt"], x["kt"], x["vt"],
+                        outs[op.REGULAR], txt[op.REGULAR], ws[op.REGULAR])
+        vds.permute(plan, b.view(N, -1), qkv_shf.view(N, -1), op.REGULAR, op.SHIFTED)
+        vds.window_attn(plan, op.SHIFTED, qkv_shf[:, 0], qkv_shf[:, 1], qkv_shf[:, 2], x["qt"], x["kt"],
+                        x["vt"], outs[op.SHIFTED], txt[op.SHIFTED], ws[op.SHIFTED])
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        layer_pair()                                   # eager, on the capture stream
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    eager = [t.clone() for t in (outs[op.REGULAR], outs[op.SHIFTED], txt[op.REGULAR], txt[op.SHIFTED])]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        layer_pair()
+    for t in list(outs.values()) + list(txt.values()):
+        t.fill_(float("nan"))
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    for got, want in zip((outs[op.REGULAR], outs[op.SHIFTED], txt[op.REGULAR], txt[op.SHIFTED]), eager):
+        assert torch.equal(got, want)
+    plan.close()
