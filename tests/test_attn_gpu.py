@@ -257,3 +257,36 @@ def test_layer_pair_replays_in_a_cuda_graph(vds):
     for got, want in zip((outs[op.REGULAR], outs[op.SHIFTED], txt[op.REGULAR], txt[op.SHIFTED]), eager):
         assert torch.equal(got, want)
     plan.close()
+
+
+def test_outputs_aligned_to_16_bytes_only(vds):
+    """o_vid starting 16 bytes into its buffer with a row stride of 16 mod 32
+    bytes, and a workspace 16 bytes past a 32-byte boundary: the epilogue
+    takes its 16-byte store path; results and guard bytes as usual."""
+    from video_dit_shifted_gb300 import synth
+    grid, heads, hd, L = (3, 30, 40, 2, 3, 3), 2, 128, 16
+    plan = vds.Plan(*grid, device="cuda")
+    N = plan.N
+    stride = heads * hd + 8                     # elements: 528 bytes per row
+    for layout in (op.REGULAR, op.SHIFTED):
+        x = synth.attention_inputs(N, L, heads, hd, torch.bfloat16, "cuda", base_seed=13)
+        buf = torch.full((N * stride + 16,), 7.0, dtype=torch.bfloat16, device="cuda")
+        o = buf[8:].as_strided((N, heads, hd), (stride, hd, 1))
+        assert o.data_ptr() % 32 == 16 and (stride * 2) % 32 == 16
+        t = torch.empty((L, heads, hd), dtype=torch.bfloat16, device="cuda")
+        need = vds.workspace_bytes(plan, layout, heads, hd, L, vds.BF16)
+        ws_buf = torch.empty(need + 64, dtype=torch.uint8, device="cuda")
+        skip = (16 - ws_buf.data_ptr()) % 32
+        ws = ws_buf[skip:skip + need]
+        assert ws.data_ptr() % 32 == 16
+        vds.window_attn(plan, layout, x["q"], x["k"], x["v"], x["qt"], x["kt"], x["vt"], o, t, ws)
+        assert vds.read_status(ws) == 0
+        off, ids = op.layout_tables(*grid, layout)
+        ref_o, ref_t = oa.window_attention(*(_np(x[n]) for n in ("q", "k", "v", "qt", "kt", "vt")), off, ids)
+        assert np.abs(_np(o) - ref_o).max() <= TOL[torch.bfloat16]
+        assert np.abs(_np(t) - oa.text_mean(ref_t)).max() <= TOL[torch.bfloat16]
+        guard = buf[:8].float()
+        assert torch.all(guard == 7.0)
+        gaps = buf[8:8 + N * stride].view(N, stride)[:, heads * hd:]
+        assert torch.all(gaps.float() == 7.0)
+    plan.close()
