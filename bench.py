@@ -472,6 +472,28 @@ def run_ours(args):
     rope = {"bound": "hbm", "achieved": rope_bytes / (rope_ms * 1e-3) / 1e9, "peak": peaks_r["hbm_gbs"],
             "unit": "GB/s", "frac": rope_bytes / (rope_ms * 1e-3) / 1e9 / peaks_r["hbm_gbs"], "ms": rope_ms,
             "bytes_per_launch": rope_bytes, "kernel": "rope_kernel (regular layout, q and k in place)"}
+    # The same regular layer with the RoPE applied inside the attention kernel
+    # (wp_window_attn_rope, un-rotated q/k in) against the RoPE pass followed
+    # by the attention call above.
+    ws_rope = vds.make_workspace(wl.plan, vds.REGULAR, wl.w["heads"], wl.w["hd"], wl.w["L"], vds.BF16, dev,
+                                 rope=True)
+    fused = lambda: vds.window_attn_rope(wl.plan, vds.REGULAR, b[:, 0], b[:, 1], b[:, 2], t[:, 0], t[:, 1],
+                                         t[:, 2], wl.o_vid[vds.REGULAR], wl.o_txt[vds.REGULAR], ws_rope)
+    for _ in range(2):
+        fused()
+    r0.record()
+    for _ in range(10):
+        fused()
+    r1.record()
+    torch.cuda.synchronize()
+    fused_ms = r0.elapsed_time(r1) / 10
+    if vds.read_status(ws_rope) != 0:
+        raise RuntimeError("device status set by wp_window_attn_rope")
+    attn_reg_ms = sum(attn_reg) / args.steps
+    rope_fused = {"kernel": "attn_tc_kernel with RoPE warps (wp_window_attn_rope), regular layer",
+                  "ms_fused": fused_ms, "tflops_fused": f_reg / (fused_ms * 1e-3) / 1e12,
+                  "ms_rope_then_attn": rope_ms + attn_reg_ms, "ms_attn": attn_reg_ms, "ms_rope": rope_ms}
+    del ws_rope
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tf, pairs, fl, secs = oracle_sample(args.workload, args.cpu_budget_s)
@@ -488,6 +510,7 @@ def run_ours(args):
                            "parallelism": "replicas" if world > 1 else "single GPU"},
                 "attn_tflops": attn_tflops, "relayout_gbs": relayout_gbs,
                 "roofline": roofline, "roofline_relayout": relayout, "roofline_rope": rope,
+                "rope_fused": rope_fused,
                 "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": wl.launches_per_step * args.steps, "clocks": clk}
         print(json.dumps(line), flush=True)

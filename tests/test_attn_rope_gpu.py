@@ -1,0 +1,143 @@
+"""wp_window_attn_rope (window attention with the window-local RoPE applied
+inside the kernel) against the oracle's RoPE followed by the oracle's window
+attention (gpu).
+
+Tolerance: bf16, max abs error <= 2e-2 against the float64 oracle fed the same
+un-rotated input bits (the kernel rotates in bf16 arithmetic)."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as oa
+from oracle import plan as op
+from oracle import rope as orp
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-2
+
+
+@pytest.fixture(scope="module")
+def vds():
+    import __graft_entry__
+    __graft_entry__.build()
+    import video_dit_shifted_gb300 as m
+    return m
+
+
+def _np(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def _oracle(grid, layout, raw, L, base=10000.0):
+    pv, pt = orp.positions(*grid, layout, L)
+    q, k = orp.rope(raw["q"], pv, base), orp.rope(raw["k"], pv, base)
+    qt, kt = (orp.rope(raw["qt"], pt, base), orp.rope(raw["kt"], pt, base)) if L else (raw["qt"], raw["kt"])
+    off, ids = op.layout_tables(*grid, layout)
+    ref_o, ref_t = oa.window_attention(q, k, raw["v"], qt, kt, raw["vt"], off, ids)
+    return ref_o, (oa.text_mean(ref_t) if L else None)
+
+
+@pytest.mark.parametrize("grid,heads,L", [
+    ((3, 30, 40, 2, 3, 3), 2, 16),      # ragged windows in both layouts, one text tile
+    ((2, 45, 80, 1, 3, 3), 1, 300),     # 720p-like frame, three text tiles (ragged)
+    ((5, 16, 24, 2, 1, 1), 3, 0),       # no text; odd window counts
+])
+def test_rope_attention_matches_oracle(vds, grid, heads, L):
+    from video_dit_shifted_gb300 import synth
+    plan = vds.Plan(*grid, device="cuda")
+    N = plan.N
+    for layout in (op.REGULAR, op.SHIFTED):
+        x = synth.attention_inputs(N, max(L, 1), heads, 128, torch.bfloat16, "cuda", base_seed=7 * layout)
+        raw = {n: _np(x[n]) for n in ("q", "k", "v", "qt", "kt", "vt")}
+        if not L:
+            for n in ("qt", "kt", "vt"):
+                raw[n] = raw[n][:0]
+        before = {n: x[n].clone() for n in ("q", "k", "qt", "kt")}
+        o = torch.full((N, heads, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+        t = torch.full((max(L, 1), heads, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+        ws = vds.make_workspace(plan, layout, heads, 128, L, vds.BF16, "cuda", rope=True)
+        args = (x["qt"][:L], x["kt"][:L], x["vt"][:L]) if L else (None, None, None)
+        vds.window_attn_rope(plan, layout, x["q"], x["k"], x["v"], *args, o, t[:L] if L else None, ws)
+        assert vds.read_status(ws) == 0
+        ref_o, ref_t = _oracle(grid, layout, raw, L)
+        assert np.abs(_np(o) - ref_o).max() <= TOL, layout
+        if L:
+            assert np.abs(_np(t[:L]) - ref_t).max() <= TOL, layout
+        for n, b in before.items():          # the inputs are not rotated in place
+            assert torch.equal(x[n], b), n
+    plan.close()
+
+
+def test_rope_attention_agrees_with_rope_pass(vds):
+    """Same layer through wp_rope + wp_window_attn_to: the two agree within
+    the bf16 tolerance, in every output layout."""
+    from video_dit_shifted_gb300 import synth
+    grid, heads, L = (3, 30, 40, 2, 3, 3), 2, 40
+    plan = vds.Plan(*grid, device="cuda")
+    N = plan.N
+    for layout in (op.REGULAR, op.SHIFTED):
+        for out_layout in (op.CANONICAL, op.REGULAR, op.SHIFTED):
+            x = synth.attention_inputs(N, L, heads, 128, torch.bfloat16, "cuda", base_seed=3)
+            o1 = torch.empty((N, heads, 128), dtype=torch.bfloat16, device="cuda")
+            t1 = torch.empty((L, heads, 128), dtype=torch.bfloat16, device="cuda")
+            ws1 = vds.make_workspace(plan, layout, heads, 128, L, vds.BF16, "cuda", rope=True)
+            vds.window_attn_rope(plan, layout, x["q"], x["k"], x["v"], x["qt"], x["kt"], x["vt"], o1, t1, ws1,
+                                 out_layout=out_layout)
+            assert vds.read_status(ws1) == 0
+            vds.rope(plan, layout, x["q"], x["k"], x["qt"], x["kt"])
+            o2 = torch.empty_like(o1)
+            t2 = torch.empty_like(t1)
+            ws2 = vds.make_workspace(plan, layout, heads, 128, L, vds.BF16, "cuda")
+            vds.window_attn(plan, layout, x["q"], x["k"], x["v"], x["qt"], x["kt"], x["vt"], o2, t2, ws2,
+                            out_layout=out_layout)
+            assert (o1.float() - o2.float()).abs().max().item() <= TOL
+            assert (t1.float() - t2.float()).abs().max().item() <= TOL
+    plan.close()
+
+
+def test_rope_attention_text_stride_and_rejections(vds):
+    """Text q/k/v inside a wider buffer (row stride > heads*128*2); then the
+    cases the call refuses before launching anything."""
+    from video_dit_shifted_gb300 import synth
+    grid, heads, L = (3, 30, 40, 2, 3, 3), 2, 20
+    plan = vds.Plan(*grid, device="cuda")
+    N = plan.N
+    layout = op.SHIFTED
+    x = synth.attention_inputs(N, L, heads, 128, torch.bfloat16, "cuda", base_seed=21)
+    wide = torch.zeros((L, 3, heads + 1, 128), dtype=torch.bfloat16, device="cuda")
+    wide[:, 0, :heads], wide[:, 1, :heads], wide[:, 2, :heads] = x["qt"], x["kt"], x["vt"]
+    qt, kt, vt = wide[:, 0, :heads], wide[:, 1, :heads], wide[:, 2, :heads]
+    raw = {n: _np(x[n]) for n in ("q", "k", "v", "qt", "kt", "vt")}
+    o = torch.empty((N, heads, 128), dtype=torch.bfloat16, device="cuda")
+    t = torch.empty((L, heads, 128), dtype=torch.bfloat16, device="cuda")
+    ws = vds.make_workspace(plan, layout, heads, 128, L, vds.BF16, "cuda", rope=True)
+    vds.window_attn_rope(plan, layout, x["q"], x["k"], x["v"], qt, kt, vt, o, t, ws)
+    assert vds.read_status(ws) == 0
+    ref_o, ref_t = _oracle(grid, layout, raw, L)
+    assert np.abs(_np(o) - ref_o).max() <= TOL
+    assert np.abs(_np(t) - ref_t).max() <= TOL
+
+    small = vds.make_workspace(plan, layout, heads, 128, L, vds.BF16, "cuda")   # no room for rotated text
+    with pytest.raises(vds.wp.WpError) as e:
+        vds.window_attn_rope(plan, layout, x["q"], x["k"], x["v"], x["qt"], x["kt"], x["vt"], o, t, small)
+    assert e.value.code == 1                                                    # WP_EINVAL
+    with pytest.raises(vds.wp.WpError) as e:
+        vds.window_attn_rope(plan, layout, x["q"], x["k"], x["v"], x["qt"], x["kt"], x["vt"], o, t, ws,
+                             rope_base=1.0)
+    assert e.value.code == 1
+    x64 = synth.attention_inputs(N, L, heads, 64, torch.bfloat16, "cuda")
+    o64 = torch.empty((N, heads, 64), dtype=torch.bfloat16, device="cuda")
+    t64 = torch.empty((L, heads, 64), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(vds.wp.WpError) as e:
+        vds.window_attn_rope(plan, layout, x64["q"], x64["k"], x64["v"], x64["qt"], x64["kt"], x64["vt"],
+                             o64, t64, ws)
+    assert e.value.code == 2                                                    # WP_EUNSUPPORTED
+    xf = synth.attention_inputs(N, L, heads, 128, torch.float32, "cuda")
+    of = torch.empty((N, heads, 128), dtype=torch.float32, device="cuda")
+    tf = torch.empty((L, heads, 128), dtype=torch.float32, device="cuda")
+    wsf = vds.make_workspace(plan, layout, heads, 128, L, vds.FP32, "cuda", rope=True)
+    with pytest.raises(vds.wp.WpError) as e:
+        vds.window_attn_rope(plan, layout, xf["q"], xf["k"], xf["v"], xf["qt"], xf["kt"], xf["vt"], of, tf, wsf)
+    assert e.value.code == 2
+    plan.close()

@@ -8,4 +8,5 @@ runs in libwp.so (include/wp.h); ``wp`` is its ctypes binding.
 """
 from . import wp  # noqa: F401
 from .wp import (BF16, CANONICAL, FP32, REGULAR, SHIFTED, Plan, make_workspace,  # noqa: F401
-                 permute, read_status, rope, window_attn, workspace_bytes)
+                 permute, read_status, rope, rope_workspace_bytes, window_attn, window_attn_rope,
+                 workspace_bytes)

@@ -190,9 +190,15 @@ using namespace wp;
 
 namespace {
 
-int workspace_bytes(const wp_plan* plan, int layout, int heads, int hd, int L, size_t* bytes) {
-  const int64_t part = static_cast<int64_t>(plan->lay[layout].nwin) * L * heads * hd * 4;
-  *bytes = kStatusBytes + static_cast<size_t>(part);
+// Partial text outputs T_w start at kStatusBytes; with rope, the rotated
+// text q and k (bf16, packed rows) follow them.
+int64_t partial_bytes(const wp_plan* plan, int layout, int heads, int hd, int L) {
+  return static_cast<int64_t>(plan->lay[layout].nwin) * L * heads * hd * 4;
+}
+
+int workspace_bytes(const wp_plan* plan, int layout, int heads, int hd, int L, size_t* bytes, bool rope = false) {
+  const int64_t text_rot = rope ? 2 * static_cast<int64_t>(L) * heads * hd * 2 : 0;
+  *bytes = kStatusBytes + static_cast<size_t>(partial_bytes(plan, layout, heads, hd, L) + text_rot);
   return WP_OK;
 }
 
@@ -217,14 +223,28 @@ extern "C" int wp_attn_workspace_bytes(const wp_plan* plan, int layout, int head
   return ok();
 }
 
+extern "C" int wp_attn_rope_workspace_bytes(const wp_plan* plan, int layout, int heads, int head_dim, int L,
+                                            int dtype, size_t* bytes) {
+  if (int rc = check_shape(plan, layout, heads, head_dim, L, dtype)) return rc;
+  if (!bytes) return fail(WP_EINVAL, "bytes is NULL");
+  workspace_bytes(plan, layout, heads, head_dim, L, bytes, true);
+  return ok();
+}
+
 namespace {
 
 int window_attn_impl(const wp_plan* plan, int layout, int out_layout, int heads, int head_dim, int L,
                      int dtype, const void* q, const void* k, const void* v, int64_t vid_row_stride_B,
                      const void* qt, const void* kt, const void* vt, int64_t txt_row_stride_B,
                      void* o_vid, int64_t o_vid_row_stride_B, void* o_txt, void* workspace,
-                     size_t ws_bytes, float softmax_scale, void* stream) {
+                     size_t ws_bytes, float softmax_scale, void* stream, float rope_base = 0.f) {
+  const bool rope = rope_base != 0.f;
   if (int rc = check_shape(plan, layout, heads, head_dim, L, dtype)) return rc;
+  if (rope) {
+    if (!(rope_base > 1.f)) return fail(WP_EINVAL, "rope_base must be > 1");
+    if (dtype != WP_BF16 || head_dim != 128)
+      return fail(WP_EUNSUPPORTED, "RoPE attention supports bf16 with head_dim 128");
+  }
   if (out_layout < 0 || out_layout >= kNumLayouts) return fail(WP_EINVAL, "bad output layout %d", out_layout);
   if (!q || !k || !v || !o_vid || !workspace) return fail(WP_EINVAL, "q, k, v, o_vid or workspace is NULL");
   if (L > 0 && (!qt || !kt || !vt || !o_txt)) return fail(WP_EINVAL, "text pointers are NULL with L=%d", L);
@@ -242,7 +262,7 @@ int window_attn_impl(const wp_plan* plan, int layout, int out_layout, int heads,
                 (long long)vid_row_stride_B, (long long)txt_row_stride_B, (long long)o_vid_row_stride_B,
                 (long long)row_B);
   size_t need = 0;
-  workspace_bytes(plan, layout, heads, head_dim, L, &need);
+  workspace_bytes(plan, layout, heads, head_dim, L, &need, rope);
   if (ws_bytes < need) return fail(WP_EINVAL, "workspace too small: %zu < %zu bytes", ws_bytes, need);
   if (int rc = require_uploaded(plan)) return rc;
 
@@ -250,7 +270,7 @@ int window_attn_impl(const wp_plan* plan, int layout, int out_layout, int heads,
   AttnCall c{};
   c.layout = layout; c.heads = heads; c.hd = head_dim; c.L = L; c.dtype = dtype;
   c.q = q; c.k = k; c.v = v; c.vid_stride_B = vid_row_stride_B;
-  c.qt = qt; c.kt = kt; c.vt = vt; c.txt_stride_B = txt_row_stride_B;
+  c.qt = qt; c.kt = kt; c.vt = vt; c.txt_stride_B = txt_row_stride_B; c.vt_stride_B = txt_row_stride_B;
   c.o_vid = o_vid; c.o_stride_B = o_vid_row_stride_B; c.o_txt = o_txt;
   c.status = static_cast<int*>(workspace);
   c.partial = reinterpret_cast<float*>(static_cast<char*>(workspace) + kStatusBytes);
@@ -269,6 +289,14 @@ int window_attn_impl(const wp_plan* plan, int layout, int out_layout, int heads,
     c.ids = nullptr;
   else
     c.ids = dev_ptr<int32_t>(plan, plan->perm_off[out_layout][layout]);
+  if (rope) {
+    c.rope = true;
+    c.boxes = dev_ptr<int32_t>(plan, plan->dlay[layout].boxes);
+    c.wt = plan->wt;
+    c.wh = plan->wh;
+    c.ww = plan->ww;
+    rope_theta(rope_base, c.rope_theta);
+  }
   c.pair_off[0] = dev_ptr<int32_t>(plan, plan->dlay[layout].pair_off[0]);
   c.pair_off[1] = dev_ptr<int32_t>(plan, plan->dlay[layout].pair_off[1]);
   c.text_tiles = (L + kTileM - 1) / kTileM;
@@ -279,6 +307,17 @@ int window_attn_impl(const wp_plan* plan, int layout, int out_layout, int heads,
 
   if (int rc = cuda_check(cudaMemsetAsync(workspace, 0, kStatusBytes, c.stream), "cudaMemsetAsync(status)"))
     return rc;
+  if (rope && L > 0) {
+    // The text rows are shared by every window: rotate them once, into the
+    // workspace, and let the kernel read the copies.
+    char* rot = static_cast<char*>(workspace) + kStatusBytes + partial_bytes(plan, layout, heads, head_dim, L);
+    void* qt_rot = rot;
+    void* kt_rot = rot + static_cast<int64_t>(L) * heads * head_dim * 2;
+    if (int rc = rope_text_copy(qt, kt, txt_row_stride_B, qt_rot, kt_rot, L, heads, rope_base, c.stream)) return rc;
+    c.qt = qt_rot;
+    c.kt = kt_rot;
+    c.txt_stride_B = static_cast<int64_t>(heads) * head_dim * 2;  // vt keeps vt_stride_B
+  }
   int rc = dtype == WP_BF16 ? launch_attn_bf16_tc(c) : launch_attn_f32(c);
   if (rc) return rc;
   if (L > 0)
@@ -308,6 +347,18 @@ extern "C" int wp_window_attn_to(const wp_plan* plan, int layout, int out_layout
   return window_attn_impl(plan, layout, out_layout, heads, head_dim, L, dtype, q, k, v, vid_row_stride_B,
                           qt, kt, vt, txt_row_stride_B, o_vid, o_vid_row_stride_B, o_txt, workspace,
                           ws_bytes, softmax_scale, stream);
+}
+
+extern "C" int wp_window_attn_rope(const wp_plan* plan, int layout, int out_layout, int heads, int head_dim,
+                                   int L, int dtype, const void* q, const void* k, const void* v,
+                                   int64_t vid_row_stride_B, const void* qt, const void* kt,
+                                   const void* vt, int64_t txt_row_stride_B, void* o_vid,
+                                   int64_t o_vid_row_stride_B, void* o_txt, void* workspace,
+                                   size_t ws_bytes, float softmax_scale, float rope_base, void* stream) {
+  if (!(rope_base > 1.f)) return fail(WP_EINVAL, "rope_base must be > 1");
+  return window_attn_impl(plan, layout, out_layout, heads, head_dim, L, dtype, q, k, v, vid_row_stride_B,
+                          qt, kt, vt, txt_row_stride_B, o_vid, o_vid_row_stride_B, o_txt, workspace,
+                          ws_bytes, softmax_scale, stream, rope_base);
 }
 
 extern "C" int wp_read_status(const void* workspace, int* device_status, void* stream) {

@@ -22,7 +22,8 @@ struct AttnCall {
   const void *q, *k, *v;
   int64_t vid_stride_B;
   const void *qt, *kt, *vt;
-  int64_t txt_stride_B;
+  int64_t txt_stride_B;  // qt and kt
+  int64_t vt_stride_B;
   void* o_vid;
   int64_t o_stride_B;
   void* o_txt;
@@ -38,11 +39,25 @@ struct AttnCall {
   const int32_t* pair_off[2];  // device
   int total_pairs;             // query-tile pairs over all windows (tile kTileM)
   int text_tiles;              // ceil(L / kTileM)
+  // Window-local RoPE applied inside the kernel (wp_window_attn_rope): the
+  // text q/k passed in are already rotated.
+  bool rope = false;
+  const int32_t* boxes = nullptr;  // device: t0,t1,h0,h1,w0,w1 per window
+  int wt = 0, wh = 0, ww = 0;      // window size
+  float rope_theta[21] = {};       // base^(-2i/42)
 };
 
 // Tensor-core (tcgen05) bf16 path; head_dim 64 or 128.
 int launch_attn_bf16_tc(const AttnCall& c);
 // SIMT fp32 path (parity mode); head_dim 64 or 128.
 int launch_attn_f32(const AttnCall& c);
+
+// RoPE angles base^(-2i/42), i < 21, as wp_rope uses them.
+void rope_theta(float rope_base, float* theta21);
+// Copies L rows of text q and k (bf16, heads x 128 per row, row stride
+// txt_stride_B) to qt_out / kt_out (packed rows) and rotates the copies in
+// place with the text positions (l, l, l) of wp_rope.
+int rope_text_copy(const void* qt, const void* kt, int64_t txt_stride_B, void* qt_out, void* kt_out, int L,
+                   int heads, float rope_base, cudaStream_t stream);
 
 }  // namespace wp

@@ -68,6 +68,9 @@ namespace {
 constexpr int kBM = 128;  // query rows per tile (TMEM lanes)
 constexpr int kBN = 128;  // keys per K/V tile
 constexpr int kThreads = 320;       // warps 0-7 softmax, 8 TMA, 9 MMA
+constexpr int kRopeThreads = 384;   // RoPE kernels: + warps 10-11 rotating Q and K tiles
+constexpr int kRopeWarp0 = 10;
+constexpr int kRopePairs = 21;      // rotated pairs per axis at head_dim 128 (42 channels)
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kTmemCols = 512;
@@ -82,16 +85,19 @@ struct Cfg {
   static constexpr int kK = 2 * kTileBytes;        // K stage s at kK + s*kTileBytes
   static constexpr int kV = 4 * kTileBytes;        // V stage s at kV + s*kTileBytes
   static constexpr int kBar = 6 * kTileBytes;
+  static constexpr int kTab = kBar + 256;          // RoPE kernels: cos/sin table
   static constexpr int kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + HD;
 };
 // Both head dims request the HD=128 footprint so that exactly one CTA (and
 // one 512-column TMEM allocation) lives on an SM.
 constexpr int kSmemBytes = Cfg<128>::kBar + 256 + 1024;
+constexpr size_t kRopeMaxSmem = 227 * 1024;  // dynamic shared memory per CTA on sm_103a
 
 struct Barriers {
   uint64_t q_full, q_empty;
   uint64_t pl_full[2], pl_empty[2];  // K/V payload slots (see the producer)
   uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
+  uint64_t q_ready, pl_ready[2];     // RoPE kernels: Q / payload rotated
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort_flag;
@@ -111,6 +117,11 @@ struct TcParams {
   float scale_log2;
   int vid_v8;  // o_vid and o_stride are 32-byte aligned: 32-byte stores
   int txt_v8;  // partial is 32-byte aligned: 32-byte stores
+  // RoPE kernels only: window boxes (t0,t1,h0,h1,w0,w1 per window), the
+  // window size (rows of the cos/sin table per axis) and theta_i.
+  const int32_t* boxes;
+  int wt, wh, ww;
+  float theta[kRopePairs];
 };
 
 // ------------------------------------------------------------ PTX helpers --
@@ -333,6 +344,62 @@ __device__ __forceinline__ float row_exp(const uint32_t (&s)[128], int valid, fl
   return (a0 + a1) + (b0 + b1);
 }
 
+// Rotate one bf16 pair (x0 low, x1 high) by the angle whose cosine and
+// sine come as the bf16 pairs cc = (c, c) and ns = (-s, s):
+// (x0 c - x1 s, x1 c + x0 s).
+__device__ __forceinline__ uint32_t rot_bf16x2(uint32_t v, uint32_t cc, uint32_t ns) {
+  uint32_t sw, t, r;
+  asm("prmt.b32 %0, %1, %1, 0x1032;" : "=r"(sw) : "r"(v));
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(t) : "r"(sw), "r"(ns));
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(v), "r"(cc), "r"(t));
+  return r;
+}
+
+// Window-local RoPE, in place, of the first `nrows` rows of a 128-row x 128
+// column bf16 tile in shared memory, laid out as TMA wrote it (two 128-byte
+// swizzled boxes of 64 columns: chunk c of row r at r*128 + (c ^ (r&7))*16).
+// Row r is the window-local token tok0 + r, at (dt, dh, dw) in the window's
+// (bh x bw) row-major order; channel pair i of axis block a (42 channels
+// each: t, h, w) turns by pos_a * theta_i, pos = (L + dt, dh, dw); pair 63
+// (channels 126, 127) is left alone.  tab holds, per axis position and i,
+// (c, c) and (-s, s) as bf16 pairs: rows [0, wt) for t, then wh rows for
+// h, then ww rows for w.  64 threads, rows rt and rt + 64.
+__device__ __forceinline__ void rope_tile(uint32_t tile, int tok0, int nrows, int bh, int bw, int wt, int wh,
+                                          const uint2* tab, int rt) {
+  const int bhw = bh * bw;
+  for (int r = rt; r < nrows; r += 64) {
+    const int tok = tok0 + r;
+    const int dt = tok / bhw, rem = tok - dt * bhw;
+    const int dh = rem / bw, dw = rem - dh * bw;
+    const uint2* tr[3] = {tab + dt * kRopePairs, tab + (wt + dh) * kRopePairs, tab + (wt + wh + dw) * kRopePairs};
+    const uint32_t row = tile + r * 128;
+    // All 16 chunks of the row in flight at once, then rotate, then store.
+    uint32_t v[16][4];
+#pragma unroll
+    for (int cc = 0; cc < 16; ++cc)
+      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(v[cc][0]), "=r"(v[cc][1]), "=r"(v[cc][2]), "=r"(v[cc][3])
+                   : "r"(row + (cc >> 3) * (128 * 128) + (((cc & 7) ^ (r & 7)) << 4))
+                   : "memory");
+#pragma unroll
+    for (int cc = 0; cc < 16; ++cc)
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int pr = 4 * cc + u;
+        if (pr < 3 * kRopePairs) {
+          const uint2 cs = tr[pr / kRopePairs][pr % kRopePairs];
+          v[cc][u] = rot_bf16x2(v[cc][u], cs.x, cs.y);
+        }
+      }
+#pragma unroll
+    for (int cc = 0; cc < 16; ++cc)
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + (cc >> 3) * (128 * 128) +
+                                                                    (((cc & 7) ^ (r & 7)) << 4)),
+                   "r"(v[cc][0]), "r"(v[cc][1]), "r"(v[cc][2]), "r"(v[cc][3])
+                   : "memory");
+  }
+}
+
 // One work item: a pair of 128-row query tiles of one (window, head).
 struct Item {
   int h, w, a, n_w, vt, nkv, t0, nq;
@@ -364,8 +431,8 @@ __device__ __forceinline__ Item decode_item(const TcParams& p, int it) {
 // that all roles advance identically.
 // 10 warps put 3 warps on one SM sub-partition (16K registers each), which
 // caps a thread at 168 registers.
-template <int HD>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int HD, bool kRope>
+__global__ void __launch_bounds__(kRope ? kRopeThreads : kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_qt,
                    const __grid_constant__ CUtensorMap tm_kt, const __grid_constant__ CUtensorMap tm_vt,
@@ -395,6 +462,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(bars->o_empty[s]), 128);
     }
     mbar_init(bar(bars->mma_done), 1);
+    if (kRope) {
+      mbar_init(bar(bars->q_ready), 64);
+      for (int s = 0; s < 2; ++s) mbar_init(bar(bars->pl_ready[s]), 64);
+    }
     // A CTA of this launch already failed: skip the work so that a broken
     // launch ends quickly instead of timing out CTA after CTA.
     bars->abort_flag = *reinterpret_cast<volatile int*>(p.status) != 0;
@@ -499,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // One query tile's share of step j: O_i += P_i V_j, then S_i = Q_i K_{j+1}^T.
       // The tile index is a compile-time constant so that every phase counter
       // and TMEM address stays in registers.
-      auto tile_step = [&](auto I, int j, int s, int sn, bool more, int cs, int co) -> bool {
+      auto tile_step = [&](auto I, int j, int s, int sn, bool more, int cs, int co, uint32_t ready_parity) -> bool {
         constexpr int i = decltype(I)::value;
         if (!wait_phase(bar(bars->p_full[i]), (cs + j) & 1, abort_flag, p.status)) return false;
         // O_i is overwritten by this item's first P V: the previous item's
@@ -509,6 +580,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         issue_pv(i, s, j == 0);
         if (more) {
+          if (kRope && i == 0) {
+            if (!wait_phase(bar(bars->pl_ready[sn]), ready_parity, abort_flag, p.status)) return false;
+            tc_fence_after();
+          }
           issue_qk(i, sn);
           mma_commit(bar(bars->s_full[i]));
         } else {
@@ -520,8 +595,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int it = blockIdx.x; it < n_items && good; it += gridDim.x, ++k) {
         const Item x = decode_item(p, it);
         // payload [K_0]
-        if (!(good = wait_phase(bq_full, k & 1, abort_flag, p.status) &&
-                     wait_phase(bar(bars->pl_full[e & 1]), (e >> 1) & 1, abort_flag, p.status)))
+        // (RoPE kernels: the rotated Q and payload, released by warps 10-11.)
+        if (!(good = wait_phase(kRope ? bar(bars->q_ready) : bq_full, k & 1, abort_flag, p.status) &&
+                     wait_phase(kRope ? bar(bars->pl_ready[e & 1]) : bar(bars->pl_full[e & 1]), (e >> 1) & 1,
+                                abort_flag, p.status)))
           break;
         tc_fence_after();
         issue_qk(0, e & 1);
@@ -536,9 +613,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < x.nkv; ++j, ++e) {
           const int s = e & 1;  // payload [V_j, K_{j+1}]
           const bool more = j + 1 < x.nkv;
+          // RoPE kernels: P V needs only V_j (landed), Q K^T the rotated K_{j+1}
+          // (pl_ready, waited inside tile_step), so the rotation overlaps P V.
           if (!(good = wait_phase(bar(bars->pl_full[s]), (e >> 1) & 1, abort_flag, p.status))) break;
-          if (!(good = tile_step(std::integral_constant<int, 0>{}, j, s, s, more, cs0, co0))) break;
-          if (x.nq > 1 && !(good = tile_step(std::integral_constant<int, 1>{}, j, s, s, more, cs1, co1))) break;
+          if (!(good = tile_step(std::integral_constant<int, 0>{}, j, s, s, more, cs0, co0, (e >> 1) & 1))) break;
+          if (x.nq > 1 && !(good = tile_step(std::integral_constant<int, 1>{}, j, s, s, more, cs1, co1, (e >> 1) & 1)))
+            break;
           mma_commit(bar(bars->pl_empty[s]));
           if (j + 2 == x.nkv) mma_commit(bq_empty);  // the Q K^T just issued was the item's last
         }
@@ -554,6 +634,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       drain_wait(bar(bars->mma_done), 0);
     }
     __syncwarp();
+  } else if (kRope && warp >= kRopeWarp0) {
+    // ======================= RoPE (warps 10-11, RoPE kernels) ===========
+    // The window-local RoPE of the item's video Q tiles and of every video K
+    // tile, in shared memory between the TMA landing (q_full / pl_full) and
+    // the MMA (q_ready / pl_ready).  Text tiles arrive already rotated; V
+    // tiles pass through.  Same order as the producer, so no phase is ever
+    // more than one ahead of these waits.
+    const int rt = threadIdx.x - kRopeWarp0 * 32;  // 0..63
+    uint2* tab = reinterpret_cast<uint2*>(smem + C::kTab);
+    const int ntab = p.wt + p.wh + p.ww;
+    for (int e = rt; e < ntab * kRopePairs; e += 64) {
+      const int row = e / kRopePairs, i = e - row * kRopePairs;
+      const int pos = row < p.wt ? p.L + row : (row < p.wt + p.wh ? row - p.wt : row - p.wt - p.wh);
+      float sn, cs;
+      sincosf(static_cast<float>(pos) * p.theta[i], &sn, &cs);
+      tab[e] = make_uint2(pack_bf16(cs, cs), pack_bf16(-sn, sn));
+    }
+    asm volatile("bar.sync 1, 64;" ::: "memory");
+    int e = 0, k = 0;
+    bool good = true;
+    for (int it = blockIdx.x; it < n_items && good; it += gridDim.x, ++k) {
+      const Item x = decode_item(p, it);
+      const int bh = __ldg(p.boxes + 6 * x.w + 3) - __ldg(p.boxes + 6 * x.w + 2);
+      const int bw = __ldg(p.boxes + 6 * x.w + 5) - __ldg(p.boxes + 6 * x.w + 4);
+      if (!(good = wait_phase(bq_full, k & 1, abort_flag, p.status))) break;
+      for (int i = 0; i < x.nq; ++i) {
+        const int t = x.t0 + i;
+        if (t < x.vt)
+          rope_tile(base + C::kQ + i * C::kTileBytes, t * kBM, min(kBM, x.n_w - t * kBM), bh, bw, p.wt, p.wh, tab, rt);
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive(bar(bars->q_ready));
+      for (int pl = 0; pl <= x.nkv; ++pl, ++e) {
+        const int slot = e & 1;
+        if (!(good = wait_phase(bar(bars->pl_full[slot]), (e >> 1) & 1, abort_flag, p.status))) break;
+        if (pl < x.vt)  // this payload's K tile (K_pl) is a video tile
+          rope_tile(base + C::kK + slot * C::kTileBytes, pl * kBN, min(kBN, x.n_w - pl * kBN), bh, bw, p.wt, p.wh, tab,
+                    rt);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive(bar(bars->pl_ready[slot]));
+      }
+    }
   } else {
     // ======================= softmax + epilogue (warps 0-7) =============
     const int i = warp >> 2;        // query tile of this warpgroup
@@ -724,8 +846,9 @@ int make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int64_
   return WP_OK;
 }
 
-template <int HD>
+template <int HD, bool kRope>
 int launch(const AttnCall& c) {
+  static_assert(!kRope || HD == 128, "the RoPE kernels rotate 128-column heads");
   CUtensorMap mq, mk, mv, mqt, mkt, mvt;
   const int64_t cols = static_cast<int64_t>(c.heads) * HD;
   if (int rc = make_map(&mq, c.q, c.N, cols, c.vid_stride_B)) return rc;
@@ -734,7 +857,7 @@ int launch(const AttnCall& c) {
   if (c.L > 0) {
     if (int rc = make_map(&mqt, c.qt, c.L, cols, c.txt_stride_B)) return rc;
     if (int rc = make_map(&mkt, c.kt, c.L, cols, c.txt_stride_B)) return rc;
-    if (int rc = make_map(&mvt, c.vt, c.L, cols, c.txt_stride_B)) return rc;
+    if (int rc = make_map(&mvt, c.vt, c.L, cols, c.vt_stride_B)) return rc;
   } else {
     mqt = mq; mkt = mk; mvt = mv;  // never read: there are no text tiles
   }
@@ -755,8 +878,20 @@ int launch(const AttnCall& c) {
   p.scale_log2 = c.scale * 1.4426950408889634f;
   p.vid_v8 = (reinterpret_cast<uintptr_t>(c.o_vid) % 32 == 0) && (c.o_stride_B % 32 == 0);
   p.txt_v8 = reinterpret_cast<uintptr_t>(c.partial) % 32 == 0;
-  auto kern = attn_tc_kernel<HD>;
-  if (int rc = cuda_check(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes),
+  p.boxes = c.boxes;
+  p.wt = c.wt;
+  p.wh = c.wh;
+  p.ww = c.ww;
+  for (int i = 0; i < kRopePairs; ++i) p.theta[i] = c.rope_theta[i];
+  size_t smem = kSmemBytes;
+  if (kRope) {
+    smem = static_cast<size_t>(Cfg<HD>::kTab) + static_cast<size_t>(c.wt + c.wh + c.ww) * kRopePairs * 8 + 1024;
+    if (smem > kRopeMaxSmem)
+      return fail(WP_EUNSUPPORTED, "window %dx%dx%d too large for the RoPE table", c.wt, c.wh, c.ww);
+  }
+  auto kern = attn_tc_kernel<HD, kRope>;
+  if (int rc = cuda_check(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(smem)),
                           "cudaFuncSetAttribute(attn_tc_kernel)"))
     return rc;
   int dev = 0, sms = 0;
@@ -768,12 +903,15 @@ int launch(const AttnCall& c) {
   const int64_t items = static_cast<int64_t>(c.total_pairs) * c.heads;
   if (items > 0x7fffffff) return fail(WP_EUNSUPPORTED, "too many work items");
   const unsigned grid = static_cast<unsigned>(std::min<int64_t>(items, sms));
-  kern<<<grid, kThreads, kSmemBytes, c.stream>>>(mq, mk, mv, mqt, mkt, mvt, p);
+  kern<<<grid, kRope ? kRopeThreads : kThreads, smem, c.stream>>>(mq, mk, mv, mqt, mkt, mvt, p);
   return cuda_check(cudaGetLastError(), "attn_tc_kernel launch");
 }
 
 }  // namespace
 
-int launch_attn_bf16_tc(const AttnCall& c) { return c.hd == 64 ? launch<64>(c) : launch<128>(c); }
+int launch_attn_bf16_tc(const AttnCall& c) {
+  if (c.rope) return c.hd == 128 ? launch<128, true>(c) : fail(WP_EUNSUPPORTED, "RoPE attention needs head_dim 128");
+  return c.hd == 64 ? launch<64, false>(c) : launch<128, false>(c);
+}
 
 }  // namespace wp

@@ -20,6 +20,7 @@
 #include <algorithm>
 #include <cmath>
 
+#include "attn_internal.h"
 #include "wp_internal.h"
 
 namespace wp {
@@ -116,6 +117,37 @@ __global__ void __launch_bounds__(kWarps * 32) rope_kernel(const RopeParams p) {
 }
 
 }  // namespace
+
+void rope_theta(float rope_base, float* theta21) {
+  for (int i = 0; i < kPairsPerAxis; ++i)
+    theta21[i] = static_cast<float>(std::pow(static_cast<double>(rope_base), -2.0 * i / kAxis));
+}
+
+int rope_text_copy(const void* qt, const void* kt, int64_t txt_stride_B, void* qt_out, void* kt_out, int L,
+                   int heads, float rope_base, cudaStream_t stream) {
+  if (L <= 0) return WP_OK;
+  const size_t row_B = static_cast<size_t>(heads) * kHd * 2;
+  if (int rc = cuda_check(cudaMemcpy2DAsync(qt_out, row_B, qt, static_cast<size_t>(txt_stride_B), row_B, L,
+                                            cudaMemcpyDeviceToDevice, stream),
+                          "cudaMemcpy2DAsync(text q)"))
+    return rc;
+  if (int rc = cuda_check(cudaMemcpy2DAsync(kt_out, row_B, kt, static_cast<size_t>(txt_stride_B), row_B, L,
+                                            cudaMemcpyDeviceToDevice, stream),
+                          "cudaMemcpy2DAsync(text k)"))
+    return rc;
+  RopeParams p{};
+  p.qt = static_cast<char*>(qt_out);
+  p.kt = static_cast<char*>(kt_out);
+  p.tstride = static_cast<int64_t>(row_B);
+  p.N = 0;  // text rows only: positions (l, l, l)
+  p.L = L;
+  p.heads = heads;
+  rope_theta(rope_base, p.theta);
+  const unsigned blocks = static_cast<unsigned>((L + kWarps - 1) / kWarps);
+  rope_kernel<__nv_bfloat16><<<blocks, kWarps * 32, 0, stream>>>(p);
+  return cuda_check(cudaGetLastError(), "rope_kernel launch (text)");
+}
+
 }  // namespace wp
 
 using namespace wp;
@@ -155,8 +187,7 @@ extern "C" int wp_rope(const wp_plan* plan, int layout, int heads, int head_dim,
   p.heads = heads;
   p.H = plan->H;
   p.W = plan->W;
-  for (int i = 0; i < kPairsPerAxis; ++i)
-    p.theta[i] = static_cast<float>(std::pow(static_cast<double>(rope_base), -2.0 * i / kAxis));
+  rope_theta(rope_base, p.theta);
   int sms = 0;
   if (int rc = cuda_check(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, plan->device),
                           "cudaDeviceGetAttribute"))

@@ -43,6 +43,11 @@ SIGNATURES = {
     "wp_window_attn_to": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                    _vp, _vp, _vp, _c_i64, _vp, _vp, _vp, _c_i64,
                                    _vp, _c_i64, _vp, _vp, _c_sz, ctypes.c_float, _vp]),
+    "wp_attn_rope_workspace_bytes": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                              ctypes.POINTER(_c_sz)]),
+    "wp_window_attn_rope": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                     _vp, _vp, _vp, _c_i64, _vp, _vp, _vp, _c_i64,
+                                     _vp, _c_i64, _vp, _vp, _c_sz, ctypes.c_float, ctypes.c_float, _vp]),
     "wp_window_attn_static": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int,
                                        _vp, _vp, _vp, _c_i64, _vp, _vp, _vp, _c_i64,
                                        _vp, _c_i64, _vp, ctypes.c_float, _vp]),
@@ -215,9 +220,37 @@ def workspace_bytes(plan, layout, heads, head_dim, L, dtype_code):
     return b.value
 
 
-def make_workspace(plan, layout, heads, head_dim, L, dtype_code, device):
-    return torch.empty(workspace_bytes(plan, layout, heads, head_dim, L, dtype_code),
-                       dtype=torch.uint8, device=device)
+def rope_workspace_bytes(plan, layout, heads, head_dim, L, dtype_code):
+    b = _c_sz()
+    _check("wp_attn_rope_workspace_bytes", lib().wp_attn_rope_workspace_bytes(
+        plan.handle, layout, heads, head_dim, L, dtype_code, ctypes.byref(b)))
+    return b.value
+
+
+def make_workspace(plan, layout, heads, head_dim, L, dtype_code, device, rope=False):
+    n = (rope_workspace_bytes if rope else workspace_bytes)(plan, layout, heads, head_dim, L, dtype_code)
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def window_attn_rope(plan, layout, q, k, v, qt, kt, vt, o_vid, o_txt, workspace, rope_base=10000.0,
+                     scale=0.0, stream=None, out_layout=CANONICAL):
+    """Window attention on un-rotated q, k with the window-local RoPE applied
+    inside the kernel (wp_window_attn_rope in include/wp.h); q, k, qt, kt are
+    not modified.  Arguments as window_attn; workspace from
+    make_workspace(..., rope=True)."""
+    N, heads, hd = q.shape
+    L = qt.shape[0] if qt is not None else 0
+    es = q.element_size()
+    if not (k.stride(0) == v.stride(0) == q.stride(0)):
+        raise ValueError("q, k, v must share one row stride")
+    txt_stride = qt.stride(0) * es if L else 0
+    _check("wp_window_attn_rope", lib().wp_window_attn_rope(
+        plan.handle, layout, out_layout, heads, hd, L, _dtype_code(q),
+        _ptr(q), _ptr(k), _ptr(v), q.stride(0) * es,
+        _ptr(qt if L else None), _ptr(kt if L else None), _ptr(vt if L else None), txt_stride,
+        _ptr(o_vid), o_vid.stride(0) * es, _ptr(o_txt if L else None),
+        _ptr(workspace), workspace.numel(), float(scale), float(rope_base), _stream_ptr(stream)))
+    return o_vid, o_txt
 
 
 def window_attn(plan, layout, q, k, v, qt, kt, vt, o_vid, o_txt, workspace, scale=0.0, stream=None,
