@@ -1,8 +1,9 @@
 """CPU model of the persistent attention kernel's barrier protocol.
 
-The kernel (csrc/attn_tc.cu) coordinates a TMA producer, one MMA-issuing
-thread and two softmax warpgroups through mbarriers that are waited on by
-phase parity.  This model replays each role's sequence of waits, arrivals
+The kernel (csrc/attn_tc.cu) coordinates a TMA producer, an MMA-issuing
+warp, two softmax warpgroups (and, in the RoPE kernels, two rotating warps)
+through mbarriers that are waited on by phase parity; work items reach all
+roles through a ring of four slots filled from a global counter.  This model replays each role's sequence of waits, arrivals
 and commits (a commit arrives when the MMAs before it finish; here, at once)
 in random interleavings over real work-item lists, and checks that:
   * no interleaving deadlocks, and
@@ -34,27 +35,54 @@ def items_for(grid, L, heads, nblocks, b, layout=op.REGULAR):
     items=[pairs[it % len(pairs)] for it in range(len(pairs)*heads)]
     return items[b::nblocks]
 
-COUNT={'q_full':1,'q_empty':1,'pl_full0':1,'pl_full1':1,'pl_empty0':1,'pl_empty1':1,
-       's_full0':1,'s_full1':1,'p_full0':1,'p_full1':1,'o_full0':1,'o_full1':1,
-       'o_empty0':1,'o_empty1':1}
+NRING = 4
+
+
+def counts(rope):
+    """Arrivals that complete one phase of each barrier (the model's roles
+    stand for whole warps or warpgroups, one arrival each)."""
+    c = {b: 1 for b in ('q_full', 'q_empty', 'pl_full0', 'pl_full1', 'pl_empty0', 'pl_empty1',
+                        's_full0', 's_full1', 'p_full0', 'p_full1', 'o_full0', 'o_full1',
+                        'o_empty0', 'o_empty1', 'q_ready', 'pl_ready0', 'pl_ready1')}
+    for u in range(NRING):
+        c['item_full%d' % u] = 1
+        c['item_empty%d' % u] = 4 if rope else 3    # MMA, two softmax warpgroups (+ RoPE warps)
+    return c
+
+
+def take(u):
+    """A consumer's share of the item ring for its u-th item (or the end mark)."""
+    yield ('wait', 'item_full%d' % (u % NRING), u // NRING)
+    yield ('arrive', 'item_empty%d' % (u % NRING))
+
 
 def producer(items):
+    # Items come from a global counter; the producer publishes each index in
+    # ring slot u % 4 once the consumers have all read the index four back.
     # payload e (global): item start -> [K(g0)]; step j -> [V(g0+j), K(g0+j+1)] (K only if
     # the item has tile j+1).  Payload e lives in slot e&1; it may load once payload e-2
     # is released (its tiles use the same K/V stages).
     e=0; k=0
-    for (w,nkv,nq) in items:
+    for u in range(len(items) + 1):
+        if u >= NRING: yield ('wait', 'item_empty%d' % (u % NRING), u // NRING - 1)
+        yield ('arrive', 'item_full%d' % (u % NRING))
+        if u == len(items): break
+        (w, nkv, nq) = items[u]
         if k>0: yield ('wait','q_empty',k-1)
         yield ('arrive','q_full'); k+=1
         for p in range(nkv+1):
             if e>=2: yield ('wait','pl_empty%d'%(e&1),(e>>1)-1)
             yield ('arrive','pl_full%d'%(e&1))
             e+=1
-def mma(items):
+
+def mma(items, rope):
     e=0; k=0; cs=[0,0]; co=[0,0]
-    for (w,nkv,nq) in items:
-        yield ('wait','q_full',k)
-        yield ('wait','pl_full%d'%(e&1),e>>1)          # payload [K(0)]
+    for u in range(len(items) + 1):
+        yield from take(u)
+        if u == len(items): break
+        (w, nkv, nq) = items[u]
+        yield ('wait','q_ready' if rope else 'q_full',k)
+        yield ('wait',('pl_ready%d' if rope else 'pl_full%d')%(e&1),e>>1)   # payload [K(0)]
         for i in range(nq): yield ('commit','s_full%d'%i)
         if nkv==1: yield ('commit','q_empty')
         yield ('commit','pl_empty%d'%(e&1))            # K(0) read by the S(0) just issued
@@ -65,7 +93,9 @@ def mma(items):
             for i in range(nq):
                 yield ('wait','p_full%d'%i,cs[i]+j)
                 if j==0 and co[i]>0: yield ('wait','o_empty%d'%i,co[i]-1)
+                if rope and more and i == 0: yield ('wait','pl_ready%d'%(e&1),e>>1)   # rotated K(j+1)
                 yield ('commit',('s_full%d' if more else 'o_full%d')%i)
+            if rope and not more: yield ('wait','pl_ready%d'%(e&1),e>>1)   # RoPE warps passed it
             yield ('commit','pl_empty%d'%(e&1))        # V(j) and K(j+1) read by MMAs just issued
             if j+2==nkv: yield ('commit','q_empty')
             e+=1
@@ -74,7 +104,10 @@ def mma(items):
 
 def softmax(items,i):
     cs=0; co=0
-    for (w,nkv,nq) in items:
+    for u in range(len(items) + 1):
+        yield from take(u)
+        if u == len(items): break
+        (w, nkv, nq) = items[u]
         if i>=nq: continue
         for j in range(nkv):
             yield ('wait','s_full%d'%i,cs+j)
@@ -83,10 +116,27 @@ def softmax(items,i):
         yield ('wait','o_full%d'%i,co)
         yield ('arrive','o_empty%d'%i); co+=1
 
-def simulate(items, seed):
+def rope_warps(items):
+    # RoPE kernels: rotate the item's Q and every payload's K between the TMA
+    # landing and the MMA.
+    e=0; k=0
+    for u in range(len(items) + 1):
+        yield from take(u)
+        if u == len(items): break
+        (w, nkv, nq) = items[u]
+        yield ('wait','q_full',k); yield ('arrive','q_ready'); k+=1
+        for p in range(nkv+1):
+            yield ('wait','pl_full%d'%(e&1),e>>1)
+            yield ('arrive','pl_ready%d'%(e&1))
+            e+=1
+
+def simulate(items, seed, rope=False):
     rnd=random.Random(seed)
-    done={b:0 for b in COUNT}
-    roles=[producer(items),mma(items),softmax(items,0),softmax(items,1)]
+    need=counts(rope)
+    done={b:0 for b in need}      # completed phases
+    arr={b:0 for b in need}       # arrivals in the current phase
+    roles=[producer(items),mma(items, rope),softmax(items,0),softmax(items,1)]
+    if rope: roles.append(rope_warps(items))
     pending=[next(r,None) for r in roles]
     steps=0
     while any(p is not None for p in pending):
@@ -104,7 +154,12 @@ def simulate(items, seed):
             raise RuntimeError("DEADLOCK: %s" % pending)
         idx=rnd.choice(ready)
         op_=pending[idx]
-        if op_[0] in ('arrive','commit'): done[op_[1]]+=1
+        if op_[0] in ('arrive','commit'):
+            b = op_[1]
+            arr[b] += 1
+            if arr[b] == need[b]:
+                arr[b] = 0
+                done[b] += 1
         pending[idx]=next(roles[idx],None); steps+=1
     return steps
 
@@ -113,10 +168,38 @@ CASES = [((2, 45, 80, 1, 3, 3), 16, 2, 152), ((2, 45, 80, 1, 3, 3), 16, 2, 7), (
          ((2, 3, 200, 1, 1, 9), 0, 1, 2)]
 
 
+@pytest.mark.parametrize("rope", [False, True])
 @pytest.mark.parametrize("layout", [op.REGULAR, op.SHIFTED])
 @pytest.mark.parametrize("grid,L,heads,nb", CASES)
-def test_protocol_has_no_deadlock_and_exact_parity(grid, L, heads, nb, layout):
+def test_protocol_has_no_deadlock_and_exact_parity(grid, L, heads, nb, layout, rope):
     for b in range(min(nb, 4)):
         its = items_for(grid, L, heads, nb, b, layout)
-        for seed in range(20):
-            simulate(its, seed)
+        for seed in range(20 if not rope else 8):
+            simulate(its, seed, rope)
+
+
+def test_model_catches_an_early_release():
+    """The checker itself: with the RoPE warps, an MMA that released an item's
+    last (V-only) payload without waiting for pl_ready lets the producer
+    refill the slot while the RoPE warps are still a payload behind; the
+    model must flag that (a parity wait that aliases, or a deadlock)."""
+    its = items_for((2, 3, 200, 1, 1, 9), 0, 1, 2, 0, op.SHIFTED)
+    global mma
+    good_mma = mma
+
+    def early_release(items, rope):
+        ops = list(good_mma(items, rope))
+        out = []
+        for n, op_ in enumerate(ops):
+            if (op_[0] == 'wait' and op_[1].startswith('pl_ready') and n + 1 < len(ops)
+                    and ops[n + 1][0] == 'commit' and ops[n + 1][1].startswith('pl_empty')):
+                continue
+            out.append(op_)
+        yield from out
+    mma = early_release
+    try:
+        with pytest.raises((AssertionError, RuntimeError)):
+            for seed in range(200):
+                simulate(its, seed, rope=True)
+    finally:
+        mma = good_mma

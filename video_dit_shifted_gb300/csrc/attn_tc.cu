@@ -98,9 +98,11 @@ struct Barriers {
   uint64_t pl_full[2], pl_empty[2];  // K/V payload slots (see the producer)
   uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
   uint64_t q_ready, pl_ready[2];     // RoPE kernels: Q / payload rotated
+  uint64_t item_full[4], item_empty[4];  // ring of work-item indices (see the producer)
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort_flag;
+  int item_idx[4];
 };
 static_assert(sizeof(Barriers) <= 256, "barrier block");
 
@@ -114,6 +116,7 @@ struct TcParams {
   int64_t o_stride;  // elements
   float* partial;
   int* status;
+  int* counter;  // next work item (zero at launch)
   float scale_log2;
   int vid_v8;  // o_vid and o_stride are 32-byte aligned: 32-byte stores
   int txt_v8;  // partial is 32-byte aligned: 32-byte stores
@@ -462,6 +465,11 @@ __global__ void __launch_bounds__(kRope ? kRopeThreads : kThreads, 1)
       mbar_init(bar(bars->o_empty[s]), 128);
     }
     mbar_init(bar(bars->mma_done), 1);
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(bar(bars->item_full[s]), 1);
+      // one arrival per consumer warp: MMA, 8 softmax (+ 2 RoPE)
+      mbar_init(bar(bars->item_empty[s]), kRope ? 11 : 9);
+    }
     if (kRope) {
       mbar_init(bar(bars->q_ready), 64);
       for (int s = 0; s < 2; ++s) mbar_init(bar(bars->pl_ready[s]), 64);
@@ -485,6 +493,21 @@ __global__ void __launch_bounds__(kRope ? kRopeThreads : kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
+  // Work items are handed out dynamically: the producer warp takes the next
+  // item index from a global counter and publishes it in a ring of four
+  // slots (item_full / item_empty); every role walks the same sequence, -1
+  // ending it.  Items of one (window, head) are still taken one after the
+  // other, so CTAs working at the same time share K/V tiles through L2.
+  auto take_item = [&](int u, bool& good) -> int {
+    const int slot = u & 3;
+    good = __all_sync(0xffffffffu, wait_phase(bar(bars->item_full[slot]), (u >> 2) & 1, abort_flag, p.status));
+    if (!good) return -1;
+    const int it = *reinterpret_cast<volatile int*>(&bars->item_idx[slot]);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(bars->item_empty[slot]));
+    return it;
+  };
+
   if (warp == kProducerWarp) {
     // ======================= TMA producer ===============================
     {
@@ -497,7 +520,21 @@ __global__ void __launch_bounds__(kRope ? kRopeThreads : kThreads, 1)
       int e = 0;  // payloads issued
       int k = 0;  // items whose Q load was issued
       bool good = true;
-      for (int it = blockIdx.x; it < n_items && good; it += gridDim.x) {
+      for (int u = 0; good; ++u) {
+        const int slot = u & 3;
+        if (u >= 4 &&
+            !(good = wait_phase(bar(bars->item_empty[slot]), ((u >> 2) - 1) & 1, abort_flag, p.status)))
+          break;
+        int it = 0;
+        if (lane == 0) it = atomicAdd(p.counter, 1);
+        it = __shfl_sync(0xffffffffu, it, 0);
+        if (it >= n_items) it = -1;
+        if (lane == 0) {
+          bars->item_idx[slot] = it;
+          mbar_arrive(bar(bars->item_full[slot]));
+        }
+        __syncwarp();
+        if (it < 0) break;
         const Item x = decode_item(p, it);
         // Q smem is free once the previous item's last Q K^T has completed.
         if (k > 0 && !(good = wait_phase(bq_empty, (k - 1) & 1, abort_flag, p.status))) break;
@@ -592,7 +629,9 @@ __global__ void __launch_bounds__(kRope ? kRopeThreads : kThreads, 1)
         return true;
       };
       int e = 0;  // payloads consumed (see the producer)
-      for (int it = blockIdx.x; it < n_items && good; it += gridDim.x, ++k) {
+      for (int u = 0; good; ++u, ++k) {
+        const int it = take_item(u, good);
+        if (it < 0) break;
         const Item x = decode_item(p, it);
         // payload [K_0]
         // (RoPE kernels: the rotated Q and payload, released by warps 10-11.)
@@ -618,6 +657,12 @@ __global__ void __launch_bounds__(kRope ? kRopeThreads : kThreads, 1)
           if (!(good = wait_phase(bar(bars->pl_full[s]), (e >> 1) & 1, abort_flag, p.status))) break;
           if (!(good = tile_step(std::integral_constant<int, 0>{}, j, s, s, more, cs0, co0, (e >> 1) & 1))) break;
           if (x.nq > 1 && !(good = tile_step(std::integral_constant<int, 1>{}, j, s, s, more, cs1, co1, (e >> 1) & 1)))
+            break;
+          // RoPE kernels: the item's last payload (V only) is released only after
+          // the RoPE warps have passed it too, so that they can never fall a
+          // payload behind the producer (a parity wait would then alias).
+          if (kRope && !more &&
+              !(good = wait_phase(bar(bars->pl_ready[s]), (e >> 1) & 1, abort_flag, p.status)))
             break;
           mma_commit(bar(bars->pl_empty[s]));
           if (j + 2 == x.nkv) mma_commit(bq_empty);  // the Q K^T just issued was the item's last
@@ -654,7 +699,9 @@ __global__ void __launch_bounds__(kRope ? kRopeThreads : kThreads, 1)
     asm volatile("bar.sync 1, 64;" ::: "memory");
     int e = 0, k = 0;
     bool good = true;
-    for (int it = blockIdx.x; it < n_items && good; it += gridDim.x, ++k) {
+    for (int u = 0; good; ++u, ++k) {
+      const int it = take_item(u, good);
+      if (it < 0) break;
       const Item x = decode_item(p, it);
       const int bh = __ldg(p.boxes + 6 * x.w + 3) - __ldg(p.boxes + 6 * x.w + 2);
       const int bw = __ldg(p.boxes + 6 * x.w + 5) - __ldg(p.boxes + 6 * x.w + 4);
@@ -687,7 +734,9 @@ __global__ void __launch_bounds__(kRope ? kRopeThreads : kThreads, 1)
     const uint32_t bs = bar(bars->s_full[i]), bp = bar(bars->p_full[i]);
     int cs = 0, co = 0;
     bool good = true;
-    for (int it = blockIdx.x; it < n_items && good; it += gridDim.x) {
+    for (int u = 0; good; ++u) {
+      const int it = take_item(u, good);
+      if (it < 0) break;
       const Item x = decode_item(p, it);
       if (i >= x.nq) continue;
       float m_run = 0.f, l_run = 0.f;
@@ -875,6 +924,7 @@ int launch(const AttnCall& c) {
   p.o_stride = c.o_stride_B / 2;
   p.partial = c.partial;
   p.status = c.status;
+  p.counter = c.status + 16;  // inside the status block, cleared before every launch
   p.scale_log2 = c.scale * 1.4426950408889634f;
   p.vid_v8 = (reinterpret_cast<uintptr_t>(c.o_vid) % 32 == 0) && (c.o_stride_B % 32 == 0);
   p.txt_v8 = reinterpret_cast<uintptr_t>(c.partial) % 32 == 0;
