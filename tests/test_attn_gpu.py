@@ -290,3 +290,41 @@ def test_outputs_aligned_to_16_bytes_only(vds):
         gaps = buf[8:8 + N * stride].view(N, stride)[:, heads * hd:]
         assert torch.all(gaps.float() == 7.0)
     plan.close()
+
+
+def test_softmax_slow_paths(vds):
+    """Scores built so that every branch of the lazy rescale runs: the first
+    tile's max lies outside its first 16 columns (row sum > 2^8 at j = 0:
+    the true max is taken and the pass redone), a later tile sits ~3.8 log2
+    units above the running max (row sum > 2^8, max within 2^8: redone
+    without a rescale), and one key is ~25 log2 units higher still (O and l
+    rescaled).  One window of 10 video tiles; checked against the oracle."""
+    grid, heads, hd, L = (2, 16, 40, 1, 1, 1), 2, 128, 16
+    plan = vds.Plan(*grid, device="cuda")
+    N = plan.N
+    off, ids = op.layout_tables(*grid, op.REGULAR)
+    assert len(off) == 2 and N == 1280                 # one window, keys in layout order
+    g = torch.Generator().manual_seed(5)
+    b = torch.randn(N, generator=g) * 4.0               # score of key n = b[n] (q = e_0)
+    b[:128] = 0.0
+    b[20] = 100.0                                       # tile 0: max outside the first 16 columns
+    b[128:256] = 130.0                                  # tile 1: every p ~ 2^3.8 over the running max
+    b[300] = 300.0                                      # tile 2: ~25 log2 units higher: rescale
+    q = torch.zeros(N, heads, hd)
+    q[:, :, 0] = 1.0
+    k = torch.zeros(N, heads, hd)
+    k[:, :, 0] = b[:, None]
+    v = torch.randn(N, heads, hd, generator=g)
+    qt = torch.randn(L, heads, hd, generator=g) * 0.1
+    kt = torch.randn(L, heads, hd, generator=g)
+    vt = torch.randn(L, heads, hd, generator=g)
+    x = {n: t.to(torch.bfloat16).cuda() for n, t in dict(q=q, k=k, v=v, qt=qt, kt=kt, vt=vt).items()}
+    o = torch.full((N, heads, hd), float("nan"), dtype=torch.bfloat16, device="cuda")
+    t = torch.full((L, heads, hd), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ws = vds.make_workspace(plan, op.REGULAR, heads, hd, L, vds.BF16, "cuda")
+    vds.window_attn(plan, op.REGULAR, x["q"], x["k"], x["v"], x["qt"], x["kt"], x["vt"], o, t, ws)
+    assert vds.read_status(ws) == 0
+    ref_o, ref_t = oa.window_attention(*(_np(x[n]) for n in ("q", "k", "v", "qt", "kt", "vt")), off, ids)
+    assert np.abs(_np(o) - ref_o).max() <= TOL[torch.bfloat16]
+    assert np.abs(_np(t) - oa.text_mean(ref_t)).max() <= TOL[torch.bfloat16]
+    plan.close()

@@ -13,10 +13,12 @@
 // through L2).  Roles inside a CTA (320 threads):
 //   warps 0-3   softmax + epilogue for query tile 0, warps 4-7 for tile 1:
 //               one thread per query row (TMEM lane); one 128-column TMEM
-//               load of S per tile, row max, 2^x in the log2 domain, P
-//               written back over S as packed bf16; O is rescaled in TMEM
-//               only when a row max grows by more than 2^8 (the final O / l
-//               is exact either way); the epilogue scatters video rows to
+//               load of S per tile, 2^x in the log2 domain against the
+//               running max, P written back over S as packed bf16; O is
+//               rescaled in TMEM only when a row max grows by more than 2^8
+//               (the final O / l is exact either way), and the row max is
+//               taken only when the row sum shows that some p may exceed
+//               2^8 (sum <= 2^8 proves every p <= 2^8); the epilogue scatters video rows to
 //               their output rows and writes text rows as fp32 T_w, with
 //               32-byte stores when the output allows it (a thread writes
 //               its own row, so each store instruction touches 32 rows:
@@ -748,29 +750,41 @@ __global__ void __launch_bounds__(kRope ? kRopeThreads : kThreads, 1)
         uint32_t s[128];
         tmem_ld_x128(tS, s);
         const bool full = valid == kBN;
-        const float mx = (full ? row_max<true>(s, valid) : row_max<false>(s, valid)) * p.scale_log2;
-        // Running max with a lazy rescale: O and l move to a new max only
-        // when some row's max grew by more than 2^8; otherwise the stale max
-        // keeps every p <= 2^8, which fp32 and bf16 hold exactly enough, and
-        // the final O / l is unchanged.
+        // Lazy rescale: O and l move to a new max only when some row's max
+        // grew by more than 2^8 over the running max m_run; otherwise every
+        // p <= 2^8, which fp32 and bf16 hold exactly enough, and the final
+        // O / l is unchanged.  The exponentials are taken against m_run
+        // first (for an item's first tile, the max of its first 16 scores);
+        // a row sum <= 2^8 proves every p <= 2^8, and only when some row's
+        // sum is larger (or not finite) is S read again, the true max taken
+        // and the pass redone.
+        if (j == 0) {
+          float m16 = __uint_as_float(s[0]);
+#pragma unroll
+          for (int c = 1; c < 16; ++c) m16 = fmaxf(m16, (full || c < valid) ? __uint_as_float(s[c]) : m16);
+          m_run = m16 * p.scale_log2;
+        }
         bool rescale = false;
         float alpha = 1.f;
-        if (j == 0) {
-          m_run = mx;
-        } else if (__any_sync(0xffffffffu, mx > m_run + 8.f)) {
-          const float m_new = fmaxf(m_run, mx);
-          alpha = ex2(m_run - m_new);
-          l_run *= alpha;
-          m_run = m_new;
-          rescale = true;
-        }
-        {
-          uint32_t pk[64];
-          l_run += full ? row_exp<true>(s, valid, p.scale_log2, m_run, pk)
+        uint32_t pk[64];
+        float l_tile = full ? row_exp<true>(s, valid, p.scale_log2, m_run, pk)
+                            : row_exp<false>(s, valid, p.scale_log2, m_run, pk);
+        if (__any_sync(0xffffffffu, !(l_tile <= 256.f))) {
+          tmem_ld_x128(tS, s);
+          const float mx = (full ? row_max<true>(s, valid) : row_max<false>(s, valid)) * p.scale_log2;
+          if (__any_sync(0xffffffffu, mx > m_run + 8.f)) {
+            const float m_new = fmaxf(m_run, mx);
+            alpha = ex2(m_run - m_new);
+            l_run *= alpha;
+            m_run = m_new;
+            rescale = j > 0;  // at j == 0 the first P V overwrites O
+          }
+          l_tile = full ? row_exp<true>(s, valid, p.scale_log2, m_run, pk)
                         : row_exp<false>(s, valid, p.scale_log2, m_run, pk);
-          // P (bf16, 2 per column) overwrites S columns 0..63, already read.
-          tmem_st_x64(tS, pk);
         }
+        l_run = j == 0 ? l_tile : l_run + l_tile;
+        // P (bf16, 2 per column) overwrites S columns 0..63, already read.
+        tmem_st_x64(tS, pk);
         if (rescale) {
           // O += P V of the previous tile has completed: this tile's S was
           // committed after it.
