@@ -8,31 +8,36 @@
 // in fp32 for the ordered mean in attn.cu.
 //
 // Design.  Work items are pairs of 128-row query tiles of one (window, head);
-// a persistent grid of one CTA per SM walks them round-robin (items of one
-// (window, head) are adjacent, so CTAs busy at the same time share K/V tiles
-// through L2).  Roles inside a CTA (320 threads):
+// a persistent grid of one CTA per SM takes them from a global counter (the
+// producer warp draws the next index and hands it to every role through a
+// ring in shared memory), so the CTAs finish within a fraction of an item of
+// each other; items of one (window, head) are handed out one after the other,
+// so CTAs busy at the same time share K/V tiles through L2.  Roles inside a
+// CTA (320 threads; 384 in the RoPE kernels):
 //   warps 0-3   softmax + epilogue for query tile 0, warps 4-7 for tile 1:
 //               one thread per query row (TMEM lane); one 128-column TMEM
 //               load of S per tile, 2^x in the log2 domain against the
 //               running max, P written back over S as packed bf16; O is
-//               rescaled in TMEM only when a row max grows by more than 2^8
-//               (the final O / l is exact either way), and the row max is
-//               taken only when the row sum shows that some p may exceed
-//               2^8 (sum <= 2^8 proves every p <= 2^8); the epilogue scatters video rows to
-//               their output rows and writes text rows as fp32 T_w, with
-//               32-byte stores when the output allows it (a thread writes
-//               its own row, so each store instruction touches 32 rows:
-//               32-byte stores write whole sectors with half the
-//               instructions, +5% end to end);
+//               rescaled in TMEM only when a row max grows by more than
+//               2^8 (the final O / l is exact either way), and the row max
+//               is taken only when the row sum shows that some p may exceed
+//               2^8 (a sum <= 2^8 proves every p <= 2^8); the epilogue
+//               scatters video rows to their output rows and writes text
+//               rows as fp32 T_w, with 32-byte stores when the output allows
+//               it (a thread writes its own row, so each store instruction
+//               touches 32 rows: 32-byte stores write whole sectors with
+//               half the instructions, +5% end to end);
 //   warp 8      TMA producer (whole warp, one elected lane issues): both Q
-//               tiles of an item, then the item's K and
-//               V tiles (video tiles of the window, then text tiles) in
-//               per-step payloads [K_0], [V_0, K_1], [V_1, K_2], ... into two
-//               K and two V slots, 128-byte swizzled, 64 columns per box; the
-//               next item's loads start as soon as slots free up;
+//               tiles of an item, then the item's K and V tiles (video
+//               tiles of the window, then text tiles) in per-step payloads
+//               [K_0], [V_0, K_1], [V_1, K_2], ... into two K and two V
+//               slots, 128-byte swizzled, 64 columns per box; the next
+//               item's loads start as soon as slots free up;
 //   warp 9      TMEM allocator (512 columns: S0, S1, O0, O1) and MMA issuer:
 //               S_i = Q_i K_j^T (both operands in shared memory) and
-//               O_i += P_i V_j (P from TMEM, V MN-major).
+//               O_i += P_i V_j (P from TMEM, V MN-major);
+//   warps 10-11 (RoPE kernels only) the window-local RoPE of video Q and K
+//               tiles in shared memory between the TMA and the MMA.
 // The two query tiles share every K/V tile, and the issue order
 // S0(j) S1(j) PV0(j) S0(j+1) PV1(j) S1(j+1) ... lets one tile's softmax run
 // while the tensor core works on the other.  The issuer is the whole warp 9,
