@@ -71,6 +71,18 @@ def test_calls_validate_before_cuda(wp):
     size = ctypes.c_size_t()
     assert lib.wp_attn_workspace_bytes(plan.handle, 1, 2, 128, 16, 0, ctypes.byref(size)) == 0
     assert size.value == 256 + 9 * 16 * 2 * 128 * 4
+    # RoPE attention: the workspace adds the rotated text q and k (bf16)
+    rsize = ctypes.c_size_t()
+    assert lib.wp_attn_rope_workspace_bytes(plan.handle, 1, 2, 128, 16, 0, ctypes.byref(rsize)) == 0
+    assert rsize.value == size.value + 2 * 16 * 2 * 128 * 2
+    rargs = lambda layout, hd, dtype, ws_bytes, base: (
+        plan.handle, layout, 0, 2, hd, 16, dtype, vp(256), vp(512), vp(768), 8192, vp(1024), vp(1280), vp(1536),
+        8192, vp(4096), 8192, vp(2048), vp(1 << 30), ws_bytes, ctypes.c_float(0.0), ctypes.c_float(base), None)
+    assert lib.wp_window_attn_rope(*rargs(1, 128, 0, 1 << 30, 1.0)) == 1       # rope_base <= 1
+    assert lib.wp_window_attn_rope(*rargs(1, 128, 1, 1 << 30, 1e4)) == 2       # fp32
+    assert lib.wp_window_attn_rope(*rargs(1, 64, 0, 1 << 30, 1e4)) == 2        # head_dim 64
+    assert lib.wp_window_attn_rope(*rargs(1, 128, 0, size.value, 1e4)) == 1    # no room for the rotated text
+    assert lib.wp_window_attn_rope(*rargs(1, 128, 0, rsize.value, 1e4)) in (3, 6)  # not uploaded
     plan.close()
 
 
