@@ -301,6 +301,16 @@ int wp_window_attn_static(const wp_plan* plan, int layout, int heads, int head_d
  * synchronising `stream` first.  Returns WP_ECUDA if the copy fails. */
 int wp_read_status(const void* workspace, int* device_status, void* stream);
 
+/* wp_debug_stall_next -- test hook for the failure path: the next
+ * `launches` bf16 attention launches (wp_window_attn*, any entry point) make
+ * the MMA warp of CTA 0 wait for an mbarrier phase that nothing completes.
+ * Its bounded wait (2 s) expires: the CTA records WP_ETIMEOUT in the status
+ * word, winds down (its copies and MMAs drained, TMEM freed) and the launch
+ * ends; the other CTAs finish their own items, and the context stays
+ * usable.  The results of a stalled launch are undefined.  0 cancels.
+ * Process-wide; WP_EINVAL for a negative count. */
+int wp_debug_stall_next(int launches);
+
 /* ---------------------------------------------------------------- misc --- */
 const char* wp_last_error(void); /* never NULL; "" when there is no error */
 int wp_abi_version(void);        /* WP_ABI_VERSION */

@@ -86,6 +86,12 @@ def test_calls_validate_before_cuda(wp):
     plan.close()
 
 
+def test_debug_stall_hook_validates(wp):
+    lib = wp.lib()
+    assert lib.wp_debug_stall_next(-1) == 1
+    assert lib.wp_debug_stall_next(0) == 0
+
+
 def test_plan_info(wp):
     plan = wp.Plan(21, 68, 120, 4, 3, 3)
     assert plan.info(wp.REGULAR) == {"n_tokens": 171360, "nwin": 100, "window": (6, 15, 27),

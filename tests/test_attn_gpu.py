@@ -328,3 +328,41 @@ def test_softmax_slow_paths(vds):
     assert np.abs(_np(o) - ref_o).max() <= TOL[torch.bfloat16]
     assert np.abs(_np(t) - oa.text_mean(ref_t)).max() <= TOL[torch.bfloat16]
     plan.close()
+
+
+def test_bounded_wait_timeout_recovers(vds):
+    """A launch whose MMA warp waits for a phase that never completes (test
+    hook) ends by itself: the bounded wait expires, the status word says
+    WP_ETIMEOUT, and the next launch on the same context is correct.  Both
+    the plain and the RoPE kernel."""
+    from video_dit_shifted_gb300 import synth
+    from oracle import rope as orp
+    grid, heads, hd, L = (3, 30, 40, 2, 3, 3), 2, 128, 16
+    plan = vds.Plan(*grid, device="cuda")
+    N = plan.N
+    x = synth.attention_inputs(N, L, heads, hd, torch.bfloat16, "cuda", base_seed=17)
+    raw = {n: _np(x[n]) for n in ("q", "k", "v", "qt", "kt", "vt")}
+    off, ids = op.layout_tables(*grid, op.REGULAR)
+    o = torch.empty((N, heads, hd), dtype=torch.bfloat16, device="cuda")
+    t = torch.empty((L, heads, hd), dtype=torch.bfloat16, device="cuda")
+    ws = vds.make_workspace(plan, op.REGULAR, heads, hd, L, vds.BF16, "cuda")
+    args = (plan, op.REGULAR, x["q"], x["k"], x["v"], x["qt"], x["kt"], x["vt"], o, t)
+    vds.debug_stall_next(1)
+    vds.window_attn(*args, ws)
+    assert vds.read_status(ws) == 4                     # WP_ETIMEOUT
+    vds.window_attn(*args, ws)
+    assert vds.read_status(ws) == 0
+    ref_o, ref_t = oa.window_attention(*(raw[n] for n in ("q", "k", "v", "qt", "kt", "vt")), off, ids)
+    assert np.abs(_np(o) - ref_o).max() <= TOL[torch.bfloat16]
+    wsr = vds.make_workspace(plan, op.REGULAR, heads, hd, L, vds.BF16, "cuda", rope=True)
+    vds.debug_stall_next(1)
+    vds.window_attn_rope(*args, wsr)
+    assert vds.read_status(wsr) == 4
+    vds.window_attn_rope(*args, wsr)
+    assert vds.read_status(wsr) == 0
+    pv, pt = orp.positions(*grid, op.REGULAR, L)
+    ref_o, _ = oa.window_attention(orp.rope(raw["q"], pv), orp.rope(raw["k"], pv), raw["v"],
+                                   orp.rope(raw["qt"], pt), orp.rope(raw["kt"], pt), raw["vt"], off, ids)
+    assert np.abs(_np(o) - ref_o).max() <= TOL[torch.bfloat16]
+    vds.debug_stall_next(0)
+    plan.close()

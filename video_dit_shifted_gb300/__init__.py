@@ -7,6 +7,6 @@ the per-window text outputs averaged over the window count.  The compute
 runs in libwp.so (include/wp.h); ``wp`` is its ctypes binding.
 """
 from . import wp  # noqa: F401
-from .wp import (BF16, CANONICAL, FP32, REGULAR, SHIFTED, Plan, make_workspace,  # noqa: F401
-                 permute, read_status, rope, rope_workspace_bytes, window_attn, window_attn_rope,
-                 workspace_bytes)
+from .wp import (BF16, CANONICAL, FP32, REGULAR, SHIFTED, Plan, debug_stall_next,  # noqa: F401
+                 make_workspace, permute, read_status, rope, rope_workspace_bytes, window_attn,
+                 window_attn_rope, workspace_bytes)

@@ -361,6 +361,12 @@ extern "C" int wp_window_attn_rope(const wp_plan* plan, int layout, int out_layo
                           ws_bytes, softmax_scale, stream, rope_base);
 }
 
+extern "C" int wp_debug_stall_next(int launches) {
+  if (launches < 0) return fail(WP_EINVAL, "launches=%d < 0", launches);
+  stall_next_launches(launches);
+  return ok();
+}
+
 extern "C" int wp_read_status(const void* workspace, int* device_status, void* stream) {
   if (!workspace || !device_status) return fail(WP_EINVAL, "workspace or device_status is NULL");
   cudaStream_t s = static_cast<cudaStream_t>(stream);

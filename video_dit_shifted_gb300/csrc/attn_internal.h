@@ -51,6 +51,9 @@ struct AttnCall {
 int launch_attn_bf16_tc(const AttnCall& c);
 // SIMT fp32 path (parity mode); head_dim 64 or 128.
 int launch_attn_f32(const AttnCall& c);
+// Test hook behind wp_debug_stall_next: the next n tensor-core launches
+// stall on purpose (see attn_tc.cu).
+void stall_next_launches(int n);
 
 // RoPE angles base^(-2i/42), i < 21, as wp_rope uses them.
 void rope_theta(float rope_base, float* theta21);

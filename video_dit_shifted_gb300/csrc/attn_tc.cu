@@ -63,6 +63,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <type_traits>
 
@@ -107,6 +108,7 @@ struct Barriers {
   uint64_t q_ready, pl_ready[2];     // RoPE kernels: Q / payload rotated
   uint64_t item_full[4], item_empty[4];  // ring of work-item indices (see the producer)
   uint64_t mma_done;
+  uint64_t stall;                    // test hook: a barrier nothing arrives at
   uint32_t tmem_base;
   int abort_flag;
   int item_idx[4];
@@ -125,6 +127,7 @@ struct TcParams {
   int* status;
   int* counter;  // next work item (zero at launch)
   float scale_log2;
+  int stall;   // test hook: CTA 0's MMA warp waits on `stall` (its bounded wait expires)
   int vid_v8;  // o_vid and o_stride are 32-byte aligned: 32-byte stores
   int txt_v8;  // partial is 32-byte aligned: 32-byte stores
   // RoPE kernels only: window boxes (t0,t1,h0,h1,w0,w1 per window), the
@@ -472,6 +475,7 @@ __global__ void __launch_bounds__(kRope ? kRopeThreads : kThreads, 1)
       mbar_init(bar(bars->o_empty[s]), 128);
     }
     mbar_init(bar(bars->mma_done), 1);
+    mbar_init(bar(bars->stall), 1);
     for (int s = 0; s < 4; ++s) {
       mbar_init(bar(bars->item_full[s]), 1);
       // one arrival per consumer warp: MMA, 8 softmax (+ 2 RoPE)
@@ -639,6 +643,11 @@ __global__ void __launch_bounds__(kRope ? kRopeThreads : kThreads, 1)
       for (int u = 0; good; ++u, ++k) {
         const int it = take_item(u, good);
         if (it < 0) break;
+        // Test hook (wp_debug_stall_next): wait for a phase that never
+        // completes, so that the bounded wait expires and the CTA winds down.
+        if (p.stall && blockIdx.x == 0 && k == 0 &&
+            !(good = wait_phase(bar(bars->stall), 0, abort_flag, p.status)))
+          break;
         const Item x = decode_item(p, it);
         // payload [K_0]
         // (RoPE kernels: the rotated Q and payload, released by warps 10-11.)
@@ -885,6 +894,15 @@ __global__ void __launch_bounds__(kRope ? kRopeThreads : kThreads, 1)
 }
 
 // ------------------------------------------------------------------- host --
+// Test hook: wp_debug_stall_next(n) makes the next n launches stall.
+std::atomic<int> g_stall_launches{0};
+bool take_stall() {
+  int n = g_stall_launches.load();
+  while (n > 0)
+    if (g_stall_launches.compare_exchange_weak(n, n - 1)) return true;
+  return false;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (!fn) {
@@ -945,6 +963,7 @@ int launch(const AttnCall& c) {
   p.status = c.status;
   p.counter = c.status + 16;  // inside the status block, cleared before every launch
   p.scale_log2 = c.scale * 1.4426950408889634f;
+  p.stall = take_stall() ? 1 : 0;
   p.vid_v8 = (reinterpret_cast<uintptr_t>(c.o_vid) % 32 == 0) && (c.o_stride_B % 32 == 0);
   p.txt_v8 = reinterpret_cast<uintptr_t>(c.partial) % 32 == 0;
   p.boxes = c.boxes;
@@ -977,6 +996,8 @@ int launch(const AttnCall& c) {
 }
 
 }  // namespace
+
+void stall_next_launches(int n) { g_stall_launches.store(n < 0 ? 0 : n); }
 
 int launch_attn_bf16_tc(const AttnCall& c) {
   if (c.rope) return c.hd == 128 ? launch<128, true>(c) : fail(WP_EUNSUPPORTED, "RoPE attention needs head_dim 128");

@@ -52,6 +52,7 @@ SIGNATURES = {
                                        _vp, _vp, _vp, _c_i64, _vp, _vp, _vp, _c_i64,
                                        _vp, _c_i64, _vp, ctypes.c_float, _vp]),
     "wp_read_status": (_c_int, [_vp, ctypes.POINTER(_c_int), _vp]),
+    "wp_debug_stall_next": (_c_int, [_c_int]),
     "wp_last_error": (ctypes.c_char_p, []),
     "wp_abi_version": (_c_int, []),
 }
@@ -274,6 +275,12 @@ def window_attn(plan, layout, q, k, v, qt, kt, vt, o_vid, o_txt, workspace, scal
         _ptr(o_vid), o_vid.stride(0) * es, _ptr(o_txt if L else None),
         _ptr(workspace), workspace.numel(), float(scale), _stream_ptr(stream)))
     return o_vid, o_txt
+
+
+def debug_stall_next(launches):
+    """Test hook: the next `launches` attention launches time out on purpose
+    (wp_debug_stall_next in include/wp.h)."""
+    _check("wp_debug_stall_next", lib().wp_debug_stall_next(int(launches)))
 
 
 def read_status(workspace, stream=None):
