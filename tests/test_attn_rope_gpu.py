@@ -141,3 +141,50 @@ def test_rope_attention_text_stride_and_rejections(vds):
         vds.window_attn_rope(plan, layout, xf["q"], xf["k"], xf["v"], xf["qt"], xf["kt"], xf["vt"], of, tf, wsf)
     assert e.value.code == 2
     plan.close()
+
+
+def test_rope_attention_1080p_sampled(vds):
+    """The 1080p-like layer at full size in both layouts, launched as the
+    bench launches it: a few (window, head) pairs (first, last, smallest,
+    largest and random windows) and their text partials against the
+    oracle's RoPE followed by its window attention; every output written,
+    the text mean equal to the ordered mean of the partials, and q/k left
+    un-rotated."""
+    from video_dit_shifted_gb300 import synth
+    grid, heads, hd, L, h = (21, 68, 120, 4, 3, 3), 24, 128, 256, 7
+    plan = vds.Plan(*grid, device="cuda")
+    N = plan.N
+    x = synth.attention_inputs(N, L, heads, hd, torch.bfloat16, "cuda")
+    before = {n: x[n].clone() for n in ("q", "k", "qt", "kt")}
+    rng = np.random.default_rng(2)
+    txt = {n: _np(x[n][:, h:h + 1]) for n in ("qt", "kt", "vt")}
+    for layout in (op.REGULAR, op.SHIFTED):
+        o = torch.full((N, heads, hd), float("nan"), dtype=torch.bfloat16, device="cuda")
+        t = torch.full((L, heads, hd), float("nan"), dtype=torch.bfloat16, device="cuda")
+        ws = vds.make_workspace(plan, layout, heads, hd, L, vds.BF16, "cuda", rope=True)
+        vds.window_attn_rope(plan, layout, x["q"], x["k"], x["v"], x["qt"], x["kt"], x["vt"], o, t, ws)
+        assert vds.read_status(ws) == 0
+        assert not torch.isnan(o).any() and not torch.isnan(t).any()
+        off, ids = op.layout_tables(*grid, layout)
+        nwin, sizes = len(off) - 1, np.diff(off)
+        wins = sorted({0, nwin - 1, int(sizes.argmin()), int(sizes.argmax())} |
+                      set(rng.choice(nwin, size=3, replace=False).tolist()))
+        rows = np.concatenate([np.arange(off[w], off[w + 1]) for w in wins])
+        sel = torch.from_numpy(rows).cuda()
+        pv, pt = orp.positions(*grid, layout, L)
+        q = orp.rope(_np(x["q"][sel, h:h + 1]), pv[rows])
+        k = orp.rope(_np(x["k"][sel, h:h + 1]), pv[rows])
+        v = _np(x["v"][sel, h:h + 1])
+        qt, kt = orp.rope(txt["qt"], pt), orp.rope(txt["kt"], pt)
+        sub_off = np.concatenate([[0], np.cumsum(sizes[wins])])
+        ref_o, ref_t = oa.window_attention(q, k, v, qt, kt, txt["vt"], sub_off, np.arange(rows.size))
+        got = _np(o[torch.from_numpy(ids[rows]).cuda(), h:h + 1])
+        assert np.abs(got - ref_o).max() <= TOL, layout
+        nb = nwin * L * heads * hd * 4
+        part = ws[256:256 + nb].view(torch.float32).view(nwin, L, heads, hd)
+        for i, w in enumerate(wins):
+            assert np.abs(_np(part[w, :, h]) - ref_t[i, :, 0]).max() <= TOL, (layout, w)
+        assert (t.double() - part.double().mean(dim=0)).abs().max().item() <= 4e-3
+    for n, b in before.items():
+        assert torch.equal(x[n], b), n
+    plan.close()
