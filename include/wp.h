@@ -251,7 +251,7 @@ int wp_attn_rope_workspace_bytes(const wp_plan* plan, int layout, int heads,
  * so results agree with wp_rope followed by wp_window_attn_to to within
  * the bf16 attention tolerance, not bit for bit.
  * Supported (WP_EUNSUPPORTED otherwise): dtype WP_BF16, head_dim 128, the
- * plan's window size (wt + wh + ww) <= 205 (the cos/sin table lives in
+ * plan's window size (wt + wh + ww) <= 196 (the cos/sin table lives in
  * shared memory), the alignment rules of wp_window_attn.  WP_EINVAL:
  * rope_base <= 1, workspace smaller than wp_attn_rope_workspace_bytes, and
  * the wp_window_attn_to cases. */

@@ -79,6 +79,7 @@ constexpr int kThreads = 320;       // warps 0-7 softmax, 8 TMA, 9 MMA
 constexpr int kRopeThreads = 384;   // RoPE kernels: + warps 10-11 rotating Q and K tiles
 constexpr int kRopeWarp0 = 10;
 constexpr int kRopePairs = 21;      // rotated pairs per axis at head_dim 128 (42 channels)
+constexpr int kRopeStride = 22;     // table entries per axis position (21 + 1 pad: 16-byte pairs)
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kTmemCols = 512;
@@ -374,17 +375,22 @@ __device__ __forceinline__ uint32_t rot_bf16x2(uint32_t v, uint32_t cc, uint32_t
 // Row r is the window-local token tok0 + r, at (dt, dh, dw) in the window's
 // (bh x bw) row-major order; channel pair i of axis block a (42 channels
 // each: t, h, w) turns by pos_a * theta_i, pos = (L + dt, dh, dw); pair 63
-// (channels 126, 127) is left alone.  tab holds, per axis position and i,
-// (c, c) and (-s, s) as bf16 pairs: rows [0, wt) for t, then wh rows for
-// h, then ww rows for w.  64 threads, rows rt and rt + 64.
+// (channels 126, 127) is left alone.  tab (a shared-memory address) holds,
+// per axis position and i, (c, c) and (-s, s) as bf16 pairs, kRopeStride
+// entries of 8 bytes per position so that pairs i and i + 1 load as one
+// 16-byte word: rows [0, wt) for t, then wh rows for h, then ww rows for w.
+// inv_bhw = 1 / (bh bw) and inv_bw = 1 / bw turn the divisions into
+// multiplies.  64 threads, rows rt and rt + 64.
 __device__ __forceinline__ void rope_tile(uint32_t tile, int tok0, int nrows, int bh, int bw, int wt, int wh,
-                                          const uint2* tab, int rt) {
+                                          uint32_t tab, float inv_bhw, float inv_bw, int rt) {
   const int bhw = bh * bw;
   for (int r = rt; r < nrows; r += 64) {
     const int tok = tok0 + r;
-    const int dt = tok / bhw, rem = tok - dt * bhw;
-    const int dh = rem / bw, dw = rem - dh * bw;
-    const uint2* tr[3] = {tab + dt * kRopePairs, tab + (wt + dh) * kRopePairs, tab + (wt + wh + dw) * kRopePairs};
+    // exact: (tok + 1/2) / bhw is at least 1/(2 bhw) away from an integer
+    const int dt = __float2int_rz((static_cast<float>(tok) + 0.5f) * inv_bhw), rem = tok - dt * bhw;
+    const int dh = __float2int_rz((static_cast<float>(rem) + 0.5f) * inv_bw), dw = rem - dh * bw;
+    const uint32_t tr[3] = {tab + dt * (kRopeStride * 8), tab + (wt + dh) * (kRopeStride * 8),
+                            tab + (wt + wh + dw) * (kRopeStride * 8)};
     const uint32_t row = tile + r * 128;
     // All 16 chunks of the row in flight at once, then rotate, then store.
     uint32_t v[16][4];
@@ -395,13 +401,19 @@ __device__ __forceinline__ void rope_tile(uint32_t tile, int tok0, int nrows, in
                    : "r"(row + (cc >> 3) * (128 * 128) + (((cc & 7) ^ (r & 7)) << 4))
                    : "memory");
 #pragma unroll
-    for (int cc = 0; cc < 16; ++cc)
+    for (int a = 0; a < 3; ++a)
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int pr = 4 * cc + u;
-        if (pr < 3 * kRopePairs) {
-          const uint2 cs = tr[pr / kRopePairs][pr % kRopePairs];
-          v[cc][u] = rot_bf16x2(v[cc][u], cs.x, cs.y);
+      for (int i = 0; i < kRopePairs; i += 2) {  // pairs i and i + 1 of axis a: one 16-byte load
+        uint32_t e0, e1, e2, e3;
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(e0), "=r"(e1), "=r"(e2), "=r"(e3)
+                     : "r"(tr[a] + i * 8)
+                     : "memory");
+        const int w0 = a * kRopePairs + i;
+        v[w0 >> 2][w0 & 3] = rot_bf16x2(v[w0 >> 2][w0 & 3], e0, e1);
+        if (i + 1 < kRopePairs) {
+          const int w1 = w0 + 1;
+          v[w1 >> 2][w1 & 3] = rot_bf16x2(v[w1 >> 2][w1 & 3], e2, e3);
         }
       }
 #pragma unroll
@@ -704,13 +716,14 @@ __global__ void __launch_bounds__(kRope ? kRopeThreads : kThreads, 1)
     // more than one ahead of these waits.
     const int rt = threadIdx.x - kRopeWarp0 * 32;  // 0..63
     uint2* tab = reinterpret_cast<uint2*>(smem + C::kTab);
+    const uint32_t tab_s = base + C::kTab;
     const int ntab = p.wt + p.wh + p.ww;
     for (int e = rt; e < ntab * kRopePairs; e += 64) {
       const int row = e / kRopePairs, i = e - row * kRopePairs;
       const int pos = row < p.wt ? p.L + row : (row < p.wt + p.wh ? row - p.wt : row - p.wt - p.wh);
       float sn, cs;
       sincosf(static_cast<float>(pos) * p.theta[i], &sn, &cs);
-      tab[e] = make_uint2(pack_bf16(cs, cs), pack_bf16(-sn, sn));
+      tab[row * kRopeStride + i] = make_uint2(pack_bf16(cs, cs), pack_bf16(-sn, sn));
     }
     asm volatile("bar.sync 1, 64;" ::: "memory");
     int e = 0, k = 0;
@@ -721,11 +734,13 @@ __global__ void __launch_bounds__(kRope ? kRopeThreads : kThreads, 1)
       const Item x = decode_item(p, it);
       const int bh = __ldg(p.boxes + 6 * x.w + 3) - __ldg(p.boxes + 6 * x.w + 2);
       const int bw = __ldg(p.boxes + 6 * x.w + 5) - __ldg(p.boxes + 6 * x.w + 4);
+      const float inv_bhw = 1.f / static_cast<float>(bh * bw), inv_bw = 1.f / static_cast<float>(bw);
       if (!(good = wait_phase(bq_full, k & 1, abort_flag, p.status))) break;
       for (int i = 0; i < x.nq; ++i) {
         const int t = x.t0 + i;
         if (t < x.vt)
-          rope_tile(base + C::kQ + i * C::kTileBytes, t * kBM, min(kBM, x.n_w - t * kBM), bh, bw, p.wt, p.wh, tab, rt);
+          rope_tile(base + C::kQ + i * C::kTileBytes, t * kBM, min(kBM, x.n_w - t * kBM), bh, bw, p.wt, p.wh, tab_s,
+                    inv_bhw, inv_bw, rt);
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       mbar_arrive(bar(bars->q_ready));
@@ -733,8 +748,8 @@ __global__ void __launch_bounds__(kRope ? kRopeThreads : kThreads, 1)
         const int slot = e & 1;
         if (!(good = wait_phase(bar(bars->pl_full[slot]), (e >> 1) & 1, abort_flag, p.status))) break;
         if (pl < x.vt)  // this payload's K tile (K_pl) is a video tile
-          rope_tile(base + C::kK + slot * C::kTileBytes, pl * kBN, min(kBN, x.n_w - pl * kBN), bh, bw, p.wt, p.wh, tab,
-                    rt);
+          rope_tile(base + C::kK + slot * C::kTileBytes, pl * kBN, min(kBN, x.n_w - pl * kBN), bh, bw, p.wt, p.wh, tab_s,
+                    inv_bhw, inv_bw, rt);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         mbar_arrive(bar(bars->pl_ready[slot]));
       }
@@ -973,7 +988,7 @@ int launch(const AttnCall& c) {
   for (int i = 0; i < kRopePairs; ++i) p.theta[i] = c.rope_theta[i];
   size_t smem = kSmemBytes;
   if (kRope) {
-    smem = static_cast<size_t>(Cfg<HD>::kTab) + static_cast<size_t>(c.wt + c.wh + c.ww) * kRopePairs * 8 + 1024;
+    smem = static_cast<size_t>(Cfg<HD>::kTab) + static_cast<size_t>(c.wt + c.wh + c.ww) * kRopeStride * 8 + 1024;
     if (smem > kRopeMaxSmem)
       return fail(WP_EUNSUPPORTED, "window %dx%dx%d too large for the RoPE table", c.wt, c.wh, c.ww);
   }
