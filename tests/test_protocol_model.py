@@ -130,7 +130,9 @@ def rope_warps(items):
             yield ('arrive','pl_ready%d'%(e&1))
             e+=1
 
-def simulate(items, seed, rope=False):
+def simulate(items, seed, rope=False, lag=None):
+    """Random interleaving; a role index in `lag` is picked only when nothing
+    else is ready or with probability 1/20, so that it falls behind."""
     rnd=random.Random(seed)
     need=counts(rope)
     done={b:0 for b in need}      # completed phases
@@ -152,6 +154,8 @@ def simulate(items, seed, rope=False):
             else: ready.append(idx)
         if not ready:
             raise RuntimeError("DEADLOCK: %s" % pending)
+        if lag is not None and len(ready) > 1 and lag in ready and rnd.random() >= 0.05:
+            ready.remove(lag)
         idx=rnd.choice(ready)
         op_=pending[idx]
         if op_[0] in ('arrive','commit'):
@@ -176,6 +180,9 @@ def test_protocol_has_no_deadlock_and_exact_parity(grid, L, heads, nb, layout, r
         its = items_for(grid, L, heads, nb, b, layout)
         for seed in range(20 if not rope else 8):
             simulate(its, seed, rope)
+        for lag in range(5 if rope else 4):          # each role in turn falling behind
+            for seed in range(3):
+                simulate(its, seed, rope, lag=lag)
 
 
 def test_model_catches_an_early_release():
@@ -183,7 +190,7 @@ def test_model_catches_an_early_release():
     last (V-only) payload without waiting for pl_ready lets the producer
     refill the slot while the RoPE warps are still a payload behind; the
     model must flag that (a parity wait that aliases, or a deadlock)."""
-    its = items_for((2, 3, 200, 1, 1, 9), 0, 1, 2, 0, op.SHIFTED)
+    its = items_for((3, 30, 40, 2, 3, 3), 0, 2, 3, 1, op.SHIFTED)
     global mma
     good_mma = mma
 
@@ -200,6 +207,6 @@ def test_model_catches_an_early_release():
     try:
         with pytest.raises((AssertionError, RuntimeError)):
             for seed in range(200):
-                simulate(its, seed, rope=True)
+                simulate(its, seed, rope=True, lag=4)      # the RoPE warps fall behind
     finally:
         mma = good_mma
