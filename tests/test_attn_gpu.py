@@ -366,3 +366,27 @@ def test_bounded_wait_timeout_recovers(vds):
     assert np.abs(_np(o) - ref_o).max() <= TOL[torch.bfloat16]
     vds.debug_stall_next(0)
     plan.close()
+
+
+def test_many_heads_and_long_text(vds):
+    """40 heads and 1000 text tokens (eight text tiles, the last ragged): the
+    work-item decode over heads and the text partial layout at sizes the
+    other cases do not reach; three heads checked against the oracle in both
+    layouts, the text mean over all windows for those heads."""
+    from video_dit_shifted_gb300 import synth
+    grid, heads, hd, L = (2, 30, 40, 1, 2, 2), 40, 128, 1000
+    plan = vds.Plan(*grid, device="cuda")
+    x = synth.attention_inputs(plan.N, L, heads, hd, torch.bfloat16, "cuda", base_seed=5)
+    raw = {n: _np(x[n]) for n in ("q", "k", "v", "qt", "kt", "vt")}
+    hs = (0, 17, 39)
+    for layout in (op.REGULAR, op.SHIFTED):
+        o_vid, o_txt, ws = _run(vds, plan, layout, x, heads, hd, L, torch.bfloat16)
+        off, ids = op.layout_tables(*grid, layout)
+        ref_o, ref_t = oa.window_attention(raw["q"], raw["k"], raw["v"], raw["qt"], raw["kt"], raw["vt"], off, ids,
+                                           heads=hs)
+        got, got_t = _np(o_vid), _np(o_txt)
+        for h in hs:
+            assert np.abs(got[:, h] - ref_o[:, h]).max() <= TOL[torch.bfloat16], (layout, h)
+            assert np.abs(got_t[:, h] - oa.text_mean(ref_t)[:, h]).max() <= TOL[torch.bfloat16], (layout, h)
+        assert not torch.isnan(o_vid).any() and not torch.isnan(o_txt).any()
+    plan.close()
