@@ -434,6 +434,72 @@ def run_full_schedule(args):
     plan.close()
 
 
+def run_sweep(args):
+    """The re-layout sweep: hidden rows [N, 2560] bf16 permuted regular ->
+    shifted and back on grids 45x80 / 68x120 / 90x160 x T in {5, 21, 30}
+    (nt, nh, nw = 4, 3, 3).  Each timed launch follows an L2 flush (a write
+    of twice the L2 size); points whose footprint is under four times L2 are
+    flagged.  Bytes = 2 * N * 5120 per launch (the 4-byte table read per
+    row is not counted).  Prints one JSON line."""
+    import video_dit_shifted_gb300 as vds
+    from video_dit_shifted_gb300 import synth
+    import __graft_entry__
+    __graft_entry__.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    peaks, peak_src = load_peaks()
+    points = []
+    clocks = ClockSampler(0)
+    clocks.start()
+    for (H, W) in ((45, 80), (68, 120), (90, 160)):
+        for T in (5, 21, 30):
+            plan = vds.Plan(T, H, W, 4, 3, 3, device=dev)
+            N = plan.N
+            src = synth.hidden(N, 2560, torch.bfloat16, dev)
+            dst = torch.empty_like(src)
+            back = torch.empty_like(src)
+            nbytes = 2.0 * N * 2560 * 2
+            res = {}
+            for name, a, b, (x, y) in (("regular->shifted", vds.REGULAR, vds.SHIFTED, (src, dst)),
+                                       ("shifted->regular", vds.SHIFTED, vds.REGULAR, (dst, back))):
+                for _ in range(args.warmup):
+                    vds.permute(plan, x, y, a, b)
+                ms = []
+                for _ in range(args.steps):
+                    flush.fill_(1)
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                    vds.permute(plan, x, y, a, b)
+                    e1.record()
+                    torch.cuda.synchronize()
+                    ms.append(e0.elapsed_time(e1))
+                med = statistics.median(ms)
+                res[name] = {"ms": med, "gbs": nbytes / (med * 1e-3) / 1e9,
+                             "frac": nbytes / (med * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+            if not torch.equal(back, src):
+                raise RuntimeError("re-layout round trip is not the identity on %dx%dx%d" % (T, H, W))
+            points.append({"grid": "%dx%dx%d" % (T, H, W), "N": N, "bytes_per_launch": nbytes,
+                           "near_l2": nbytes < 4 * l2, **res})
+            plan.close()
+            del src, dst, back
+    clk = clocks.stop()
+    big = [p for p in points if not p["near_l2"]]
+    gbs = [p[d]["gbs"] for p in big for d in ("regular->shifted", "shifted->regular")]
+    line = {"metric": "re-layout GB/s (% HBM), [N,2560] bf16 sweep", "value": statistics.median(gbs),
+            "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": "re-layout sweep: hidden rows [N,2560] bf16, grids 45x80/68x120/90x160 x "
+                                   "T in {5,21,30}, nt nh nw = 4 3 3, both directions; value = median GB/s "
+                                   "over the points above 4x L2",
+                       "l2": "L2 flushed (write of %d MB) before every timed launch" % (2 * l2 // 2**20)},
+            "peak": peaks["hbm_gbs"], "peak_source": peak_src, "frac": statistics.median(gbs) / peaks["hbm_gbs"],
+            "points": points, "gpu_launches": len(points) * 2 * args.steps, "clocks": clk}
+    print(json.dumps(line), flush=True)
+
+
 def run_ours(args):
     world, rank, local, pg = dist_setup(args)
     dev = torch.device("cuda", local)
@@ -562,7 +628,7 @@ def main():
     ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS) + ["full"], default="1080p")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + ["full", "sweep"], default="1080p")
     ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--ref-step-s", type=float, default=4.0)
@@ -575,6 +641,8 @@ def main():
         run_reference(args)
     elif args.workload == "full":
         run_full_schedule(args)
+    elif args.workload == "sweep":
+        run_sweep(args)
     else:
         run_ours(args)
 
