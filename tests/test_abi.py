@@ -68,6 +68,13 @@ def test_calls_validate_before_cuda(wp):
     assert lib.wp_window_attn(*args(0, 128, 1 << 30)) == 1
     assert lib.wp_window_attn(*args(1, 96, 1 << 30)) == 2
     assert lib.wp_window_attn(*args(1, 128, 64)) == 1
+    # degenerate head and text counts
+    hargs = lambda heads, L: (plan.handle, 1, heads, 128, L, 0, vp(256), vp(512), vp(768), 8192, vp(1024),
+                              vp(1280), vp(1536), 8192, vp(4096), 8192, vp(2048), vp(1 << 30), 1 << 30,
+                              ctypes.c_float(0.0), None)
+    for heads, L in [(0, 16), (-1, 16), (1 << 20, 16), (2, -1)]:
+        assert lib.wp_window_attn(*hargs(heads, L)) == 1, (heads, L)
+        assert lib.wp_last_error()
     size = ctypes.c_size_t()
     assert lib.wp_attn_workspace_bytes(plan.handle, 1, 2, 128, 16, 0, ctypes.byref(size)) == 0
     assert size.value == 256 + 9 * 16 * 2 * 128 * 4
