@@ -215,15 +215,16 @@ def run_e2e(wl, steps, warmup):
     wp_permute, runs the step, and copies every output back (video and text
     outputs of both layers, hidden rows), all inside the timed region.
 
-    Steps are pipelined the way a serving loop would run them: two device
+    Steps are pipelined the way a serving loop would run them: three device
     buffer sets and three streams, so that the copy-in of step i+1 and the
     copy-out of step i-1 overlap step i's compute (the copy engines of the
-    two directions run at once).  Events keep every reuse safe: a set's
-    inputs are overwritten only after the compute that read them, its
-    outputs only after the copy-out that read them."""
+    two directions run at once).  Events keep every reuse safe: a set is
+    refilled only after the copy-out of its last outputs (the hidden rows
+    are both an input and an output), and its compute waits for its inputs."""
     vds = wl.vds
     N = wl.N
-    sets = [wl, Workload(wl.name, wl.dev)]
+    nsets = 3
+    sets = [wl] + [Workload(wl.name, wl.dev) for _ in range(nsets - 1)]
 
     def ins(w):
         return {"qkv_reg": w.qkv[vds.REGULAR], "txt": w.txt, "hidden": w.hidden}
@@ -239,20 +240,19 @@ def run_e2e(wl, steps, warmup):
     d2h = sum(t.numel() * t.element_size() for t in pinned_out[0])
     s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     ev = lambda: torch.cuda.Event()
-    in_done, comp_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
-    for e in comp_done + out_done:
+    in_done, comp_done, out_done = ([ev() for _ in range(nsets)] for _ in range(3))
+    for e in out_done:
         e.record(torch.cuda.current_stream())
 
     def one(i):
-        b = i % 2
+        b = i % nsets
         w = sets[b]
-        s_in.wait_event(comp_done[b])          # the compute that read this set's inputs is done
+        s_in.wait_event(out_done[b])           # this set's last outputs (and so its compute) are done
         with torch.cuda.stream(s_in):
             for k, dst in ins(w).items():
                 dst.copy_(pinned_in[k], non_blocking=True)
             in_done[b].record(s_in)
         s_comp.wait_event(in_done[b])
-        s_comp.wait_event(out_done[b])         # the copy-out of this set's outputs is done
         with torch.cuda.stream(s_comp):
             vds.permute(w.plan, w.qkv[vds.REGULAR].view(N, -1), w.qkv[vds.SHIFTED].view(N, -1),
                         vds.REGULAR, vds.SHIFTED)
@@ -279,8 +279,26 @@ def run_e2e(wl, steps, warmup):
     torch.cuda.synchronize()
     for w in sets:
         w.check_status()
-    del sets[1]
-    return start.elapsed_time(end) / steps, h2d, d2h
+    e2e_ms = start.elapsed_time(end) / steps
+    # The same copies with no compute, both directions at once: what this
+    # box's host link allows per step right now (the e2e bound).
+    w = sets[0]
+    l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    l0.record(s_in)
+    s_out.wait_stream(s_in)
+    for _ in range(3):
+        with torch.cuda.stream(s_in):
+            for k, dst in ins(w).items():
+                dst.copy_(pinned_in[k], non_blocking=True)
+        with torch.cuda.stream(s_out):
+            for o, p in zip(outs(w), pinned_out[0]):
+                p.copy_(o, non_blocking=True)
+    s_in.wait_stream(s_out)
+    l1.record(s_in)
+    torch.cuda.synchronize()
+    link_ms = l0.elapsed_time(l1) / 3
+    del sets[1:]
+    return e2e_ms, h2d, d2h, link_ms
 
 
 def oracle_sample(wl_name, budget_s, seed_rows=None):
@@ -552,12 +570,13 @@ def run_ours(args):
                 "traffic": recorded_traffic("permute.cu", "permute_1080p") if args.workload == "1080p" else None,
                 "kernel": "permute_rows_kernel", "bytes_per_launch": wl.relayout_bytes, "ms": perm_ms,
                 "peak_source": peak_src}
-    e2e_ms, h2d, d2h = run_e2e(wl, args.e2e_steps, max(1, min(args.warmup, 2)))
+    e2e_ms, h2d, d2h, link_ms = run_e2e(wl, args.e2e_steps, max(3, min(args.warmup, 4)))
     e2e_ms = max_over_ranks(pg, e2e_ms, dev)
     e2e = {"value": world * step_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
            "steps": args.e2e_steps,
-           "pipelining": "copy-in of step i+1 and copy-out of step i-1 overlap step i (2 device buffer sets, "
+           "copies_only_ms_per_step": link_ms,
+           "pipelining": "copy-in of step i+1 and copy-out of step i-1 overlap step i (3 device buffer sets, "
                          "3 streams); every step's copies are inside the timed region"}
     # Window-local RoPE of q and k (a separate in-place pass, not part of the
     # step): HBM-bound, 2 tensors x (read + write) x rows x heads x 128 x 2 B.
@@ -629,7 +648,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS) + ["full", "sweep"], default="1080p")
-    ap.add_argument("--e2e-steps", type=int, default=8)
+    ap.add_argument("--e2e-steps", type=int, default=16)
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--ref-step-s", type=float, default=4.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
