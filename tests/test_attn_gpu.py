@@ -390,3 +390,33 @@ def test_many_heads_and_long_text(vds):
             assert np.abs(got_t[:, h] - oa.text_mean(ref_t)[:, h]).max() <= TOL[torch.bfloat16], (layout, h)
         assert not torch.isnan(o_vid).any() and not torch.isnan(o_txt).any()
     plan.close()
+
+
+def test_two_streams_at_once_match_one_at_a_time(vds):
+    """Two layers (different plans, layouts and workspaces) launched on two
+    streams at the same time give bit for bit what they give alone: the
+    calls share no device state."""
+    from video_dit_shifted_gb300 import synth
+    cases = [((3, 30, 40, 2, 3, 3), op.REGULAR, 2, 20), ((2, 45, 80, 1, 3, 3), op.SHIFTED, 3, 16)]
+    runs = []
+    for grid, layout, heads, L in cases:
+        plan = vds.Plan(*grid, device="cuda")
+        x = synth.attention_inputs(plan.N, L, heads, 128, torch.bfloat16, "cuda", base_seed=layout)
+        ws = vds.make_workspace(plan, layout, heads, 128, L, vds.BF16, "cuda")
+        outs = [(torch.empty((plan.N, heads, 128), dtype=torch.bfloat16, device="cuda"),
+                 torch.empty((L, heads, 128), dtype=torch.bfloat16, device="cuda")) for _ in range(2)]
+        runs.append((plan, layout, x, ws, outs))
+    for plan, layout, x, ws, outs in runs:                 # alone, one after the other
+        vds.window_attn(plan, layout, x["q"], x["k"], x["v"], x["qt"], x["kt"], x["vt"], *outs[0], ws)
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream() for _ in runs]
+    for (plan, layout, x, ws, outs), st in zip(runs, streams):   # both at once
+        st.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(st):
+            vds.window_attn(plan, layout, x["q"], x["k"], x["v"], x["qt"], x["kt"], x["vt"], *outs[1], ws,
+                            stream=st)
+    torch.cuda.synchronize()
+    for plan, layout, x, ws, outs in runs:
+        assert vds.read_status(ws) == 0
+        assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+        plan.close()
