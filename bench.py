@@ -282,21 +282,21 @@ def run_e2e(wl, steps, warmup):
     e2e_ms = start.elapsed_time(end) / steps
     # The same copies with no compute, both directions at once: what this
     # box's host link allows per step right now (the e2e bound).
-    w = sets[0]
     l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     l0.record(s_in)
     s_out.wait_stream(s_in)
-    for _ in range(3):
+    for r in range(nsets):                 # every buffer set once, as the loop uses them
+        w = sets[r]
         with torch.cuda.stream(s_in):
             for k, dst in ins(w).items():
                 dst.copy_(pinned_in[k], non_blocking=True)
         with torch.cuda.stream(s_out):
-            for o, p in zip(outs(w), pinned_out[0]):
+            for o, p in zip(outs(w), pinned_out[r]):
                 p.copy_(o, non_blocking=True)
     s_in.wait_stream(s_out)
     l1.record(s_in)
     torch.cuda.synchronize()
-    link_ms = l0.elapsed_time(l1) / 3
+    link_ms = l0.elapsed_time(l1) / nsets
     del sets[1:]
     return e2e_ms, h2d, d2h, link_ms
 
