@@ -14,7 +14,7 @@ Follows "Window-Aligned Sequence Parallelism (SeedVR2)", §Window layouts:
   gets by windowing ``arange(T*H*W).reshape(T, H, W)`` -- and that is exactly
   how ``layout_tables`` builds the id table here.
 
-Readings of points the page leaves open (each listed in the design doc):
+Readings of points the page leaves open:
 
 * ``round`` is Python's ``round`` on the float64 product (ties to even).
 * The half-window shift of an odd window length is floored: cuts sit at

@@ -7,7 +7,7 @@ window-local (dt, dh, dw) uses axial indices (text_len + dt, dh, dw), and
 every window restarts at 0; the rotary span is 3 * (rope_dim // 3) channels
 (126 of 128), so the last two channels pass through unrotated.
 
-Readings of what the page leaves open (listed in the design doc):
+Readings of what the page leaves open:
 * the span is three equal blocks, axes t, h, w in that order (42 channels
   each at head_dim 128);
 * inside a block of d channels, channels (2i, 2i+1) form a pair rotated by
