@@ -30,7 +30,8 @@
  *     device work is asynchronous on that stream.
  *   - Faults detected on the device (a bounded wait that expired, a failed
  *     bounds check) are written to a status word in the attention workspace
- *     and read back with wp_read_status(); no kernel traps or spins forever.
+ *     (or in wp_window_attn_static's fixed scratch) and read back with
+ *     wp_read_status(); no kernel traps or spins forever.
  *   - Batch is 1: a batch of videos is more windows.
  *   - There is no CPU fallback: without a usable sm_103a device every
  *     launching call returns WP_ECUDA.
@@ -191,8 +192,9 @@ int wp_attn_workspace_bytes(const wp_plan* plan, int layout, int heads,
  *     Y = softmax(Q_X K_X^T * s) V_X     (full, no mask; s = softmax_scale,
  *                                         or 1/sqrt(head_dim) if <= 0)
  * Video rows of Y are written to o_vid at their CANONICAL row ids; the text
- * rows of Y are T_w, and o_txt = (T_0 + ... + T_{nwin-1}) / nwin, summed in
- * window order (deterministic, no atomics).
+ * rows of Y are T_w (fp32, written to the workspace), and
+ * o_txt = (T_0 + ... + T_{nwin-1}) / nwin, summed in fp32 in window order by
+ * a second kernel (deterministic, no atomics).
  * Layout (element type = dtype):
  *   q, k, v   [N, heads, head_dim] rows in `layout` order; row r of q starts
  *             at q + r*vid_row_stride_B (q, k, v share the stride, e.g. a
@@ -271,22 +273,28 @@ int wp_window_attn_rope(const wp_plan* plan, int layout, int out_layout, int hea
  * allocator at hand).  The pages define nothing like it: it is a convenience
  * of this library with no counterpart in the method.
  * Same arguments, layout and results as wp_window_attn, minus the workspace:
- * the scratch (status block + per-window text outputs) comes from one
- * array of WP_STATIC_SCRATCH_BYTES bytes compiled into the library's device
- * image, which every GPU that loads the library holds until the process
- * exits.  The call allocates nothing and calls no allocating routine.
+ * the scratch comes from one array of WP_STATIC_SCRATCH_BYTES bytes compiled
+ * into the library's device image.  The call allocates nothing and calls no
+ * allocating routine.
  *   - Size limit: the call needs 256 + nwin*L*heads*head_dim*4 bytes of
  *     scratch (wp_attn_workspace_bytes); larger requests return
  *     WP_EUNSUPPORTED with a message, and nothing is launched.
  *   - Set-up: the first call on each device looks up the array's device
  *     address (cudaGetSymbolAddress) with that device current and remembers
- *     it; make that first call before capturing any stream into a graph.
+ *     it.  With CUDA's lazy module loading (the default) that lookup is also
+ *     when the runtime loads the library's device code onto the device and
+ *     reserves the array, so the first call may take device memory and can
+ *     fail with WP_ECUDA if none is left: make it before a fixed pool claims
+ *     the device, and before capturing any stream into a graph.  Later calls
+ *     allocate nothing.  Only devices on which this set-up ran hold the
+ *     array (until the process exits).  After cudaDeviceReset the remembered
+ *     address is stale: do not call this entry point on that device again.
  *   - Sharing: every call on a device uses the same array, which keeps the
  *     last call's contents (the call clears what must start at zero).  Calls
  *     whose work overlaps on the GPU (e.g. on two streams at once) race on
  *     it: order them on one stream or synchronise between them.
- *   - The device status word is not readable by the caller; a bounded wait
- *     that expires still ends the kernel. */
+ *   - Device faults: wp_read_status(NULL, ...) reads the array's status
+ *     word (WP_ETIMEOUT after a bounded wait expired) like a workspace's. */
 #define WP_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
 int wp_window_attn_static(const wp_plan* plan, int layout, int heads, int head_dim,
                           int L, int dtype, const void* q, const void* k,
@@ -298,7 +306,10 @@ int wp_window_attn_static(const wp_plan* plan, int layout, int heads, int head_d
 
 /* wp_read_status -- copies the device status word of `workspace` to
  * *device_status (a wp_status value: WP_OK, WP_ETIMEOUT or WP_EDEVICE),
- * synchronising `stream` first.  Returns WP_ECUDA if the copy fails. */
+ * synchronising `stream` first.  workspace == NULL reads the status word of
+ * wp_window_attn_static's fixed scratch on the current device (the set-up
+ * described there happens here if it has not yet).  No device memory is
+ * allocated.  Returns WP_ECUDA if the copy fails. */
 int wp_read_status(const void* workspace, int* device_status, void* stream);
 
 /* wp_debug_stall_next -- test hook for the failure path: the next

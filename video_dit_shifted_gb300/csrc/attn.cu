@@ -368,7 +368,13 @@ extern "C" int wp_debug_stall_next(int launches) {
 }
 
 extern "C" int wp_read_status(const void* workspace, int* device_status, void* stream) {
-  if (!workspace || !device_status) return fail(WP_EINVAL, "workspace or device_status is NULL");
+  if (!device_status) return fail(WP_EINVAL, "device_status is NULL");
+  if (!workspace) {
+    // The fixed scratch of wp_window_attn_static on the current device.
+    void* scratch = nullptr;
+    if (int rc = static_scratch_address(&scratch)) return rc;
+    workspace = scratch;
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int host = 0;
   if (int rc = cuda_check(cudaMemcpyAsync(&host, workspace, sizeof(int), cudaMemcpyDeviceToHost, s),

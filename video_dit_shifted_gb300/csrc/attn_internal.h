@@ -55,6 +55,10 @@ int launch_attn_f32(const AttnCall& c);
 // stall on purpose (see attn_tc.cu).
 void stall_next_launches(int n);
 
+// Device address of the fixed scratch of wp_window_attn_static on the
+// current device (looked up, and remembered, on the first call per device).
+int static_scratch_address(void** out);
+
 // RoPE angles base^(-2i/42), i < 21, as wp_rope uses them.
 void rope_theta(float rope_base, float* theta21);
 // Copies L rows of text q and k (bf16, heads x 128 per row, row stride

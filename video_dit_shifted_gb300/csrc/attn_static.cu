@@ -13,8 +13,14 @@
 // The array's name means something different on the host than on the
 // device: host code only sees a stand-in symbol.  Its real device address is
 // asked from the runtime (cudaGetSymbolAddress) the first time this entry
-// point runs on a device, with that device current, and is remembered per
-// device; the kernels then receive that address like any workspace pointer.
+// point (or wp_read_status with a NULL workspace) runs on a device, with that
+// device current, and is remembered per device; the kernels then receive
+// that address like any workspace pointer.  Under CUDA's lazy module loading
+// that first lookup is also when the runtime loads this module onto the
+// device and reserves the array, so the first call is the set-up; every
+// later call reuses the remembered address and allocates nothing.  A
+// cudaDeviceReset unloads the module: the remembered address is then stale,
+// and this entry point must not be used on that device again in the process.
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -30,8 +36,12 @@ constexpr int kMaxDevices = 64;
 std::atomic<void*> g_scratch_addr[kMaxDevices];
 std::mutex g_setup_mutex;
 
+}  // namespace
+
+namespace wp {
+
 // Device address of g_static_scratch on the current device (looked up once).
-int scratch_address(void** out) {
+int static_scratch_address(void** out) {
   int dev = -1;
   if (int rc = wp::cuda_check(cudaGetDevice(&dev), "cudaGetDevice")) return rc;
   if (dev < 0 || dev >= kMaxDevices)
@@ -52,7 +62,7 @@ int scratch_address(void** out) {
   return WP_OK;
 }
 
-}  // namespace
+}  // namespace wp
 
 extern "C" int wp_window_attn_static(const wp_plan* plan, int layout, int heads, int head_dim, int L,
                                      int dtype, const void* q, const void* k, const void* v,
@@ -68,7 +78,7 @@ extern "C" int wp_window_attn_static(const wp_plan* plan, int layout, int heads,
                     "allocation-free entry point has %zu; use wp_window_attn with a workspace",
                     need, static_cast<size_t>(WP_STATIC_SCRATCH_BYTES));
   void* scratch = nullptr;
-  if (int rc = scratch_address(&scratch)) return rc;
+  if (int rc = wp::static_scratch_address(&scratch)) return rc;
   // wp_window_attn clears the status block itself at the start of the call;
   // the text partials are fully overwritten before they are read.
   return wp_window_attn(plan, layout, heads, head_dim, L, dtype, q, k, v, vid_row_stride_B, qt, kt, vt,
