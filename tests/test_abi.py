@@ -76,8 +76,12 @@ def test_calls_validate_before_cuda(wp):
         assert lib.wp_window_attn(*hargs(heads, L)) == 1, (heads, L)
         assert lib.wp_last_error()
     size = ctypes.c_size_t()
+    # status block, per-window text outputs [9, 16, 2, 128] fp32 (either dtype)
     assert lib.wp_attn_workspace_bytes(plan.handle, 1, 2, 128, 16, 0, ctypes.byref(size)) == 0
     assert size.value == 256 + 9 * 16 * 2 * 128 * 4
+    fsize = ctypes.c_size_t()
+    assert lib.wp_attn_workspace_bytes(plan.handle, 1, 2, 128, 16, 1, ctypes.byref(fsize)) == 0
+    assert fsize.value == size.value
     # RoPE attention: the workspace adds the rotated text q and k (bf16)
     rsize = ctypes.c_size_t()
     assert lib.wp_attn_rope_workspace_bytes(plan.handle, 1, 2, 128, 16, 0, ctypes.byref(rsize)) == 0

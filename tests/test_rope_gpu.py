@@ -1,4 +1,15 @@
-"""wp_rope (window-local 3D RoPE, in place) against the oracle (gpu)."""
+"""wp_rope (window-local 3D RoPE, in place) against the oracle (gpu).
+
+Tolerances.  bf16: 2e-2 max abs, as for attention.  fp32: 1e-4 max abs.
+Basis of the fp32 figure: the kernel forms each angle as float(pos) *
+theta_i in fp32, with theta_i = base^(-2i/42) rounded once to fp32 on the
+host, so the angle carries at most 2 * 2^-24 * |pos * theta_i| of error
+(the oracle's angles are float64), and sincosf adds a few ulp; a rotated
+value x0 c - x1 s is then off by at most (|x0| + |x1|) * (angle error +
+2^-22) plus the rounding of two products and a sum.  On these grids
+|pos * theta_i| <= 39 (the canonical layout's widest axis) and |x| < 6 for
+N(0,1) draws of this size, which bounds the error near 4e-5.
+"""
 import numpy as np
 import pytest
 import torch
@@ -9,7 +20,7 @@ from oracle import rope as orp
 
 pytestmark = pytest.mark.gpu
 
-TOL = {torch.bfloat16: 2e-2, torch.float32: 5e-4}
+TOL = {torch.bfloat16: 2e-2, torch.float32: 1e-4}
 
 
 @pytest.fixture(scope="module")
