@@ -12,9 +12,13 @@ Inputs are synthetic N(0,1) (seeded) and resident in HBM before the timed
 region; every input is larger than L2, so no flush is needed between steps.
 The headline value is attention TFLOP/s over the whole step time (permutes
 included); the kernel-level numbers and the roofline are reported beside it.
+On one GPU the same line also carries the metric's 720p-like layers
+(attn_720p), a bounded run of the re-layout sweep (relayout_sweep) and a
+short run of the 32-layer schedule on T=30, 90x160 with the fused re-layout
+beside the unfused one (full_schedule); --no-extras leaves them out.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload 1080p|720p]
+                  [--workload 1080p|720p|full|sweep] [--no-extras]
 
 --impl reference times the CPU oracle on the host cores (bounded samples of
 the same workload, same metric and unit).  Under torchrun every rank runs an
@@ -153,7 +157,7 @@ def max_over_ranks(pg, x, device):
 
 # ------------------------------------------------------------------ ours --
 class Workload:
-    def __init__(self, name, device):
+    def __init__(self, name, device, hidden=True):
         import video_dit_shifted_gb300 as vds
         from video_dit_shifted_gb300 import synth
         self.vds, self.w, self.name, self.dev = vds, WORKLOADS[name], name, device
@@ -166,8 +170,9 @@ class Workload:
         vds.permute(self.plan, x["vid_buf"].view(N, -1), self.qkv[vds.SHIFTED].view(N, -1),
                     vds.REGULAR, vds.SHIFTED)
         self.txt = x["txt_buf"]
-        self.hidden = synth.hidden(N, w["hidden"], torch.bfloat16, device)
-        self.hidden2 = torch.empty_like(self.hidden)
+        if hidden:
+            self.hidden = synth.hidden(N, w["hidden"], torch.bfloat16, device)
+            self.hidden2 = torch.empty_like(self.hidden)
         self.o_vid = {l: torch.empty((N, heads, hd), dtype=torch.bfloat16, device=device)
                       for l in (vds.REGULAR, vds.SHIFTED)}
         self.o_txt = {l: torch.empty((L, heads, hd), dtype=torch.bfloat16, device=device)
@@ -264,9 +269,30 @@ def run_e2e(wl, steps, warmup):
                 p.copy_(o, non_blocking=True)
             out_done[b].record(s_out)
 
+    def copies_only():
+        """The same copies with no compute, both directions at once, every
+        buffer set once as the loop uses them: what the host link allows per
+        step at that moment (the e2e bound)."""
+        l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        l0.record(s_in)
+        s_out.wait_stream(s_in)
+        for r in range(nsets):
+            w = sets[r]
+            with torch.cuda.stream(s_in):
+                for k, dst in ins(w).items():
+                    dst.copy_(pinned_in[k], non_blocking=True)
+            with torch.cuda.stream(s_out):
+                for o, p in zip(outs(w), pinned_out[r]):
+                    p.copy_(o, non_blocking=True)
+        s_in.wait_stream(s_out)
+        l1.record(s_in)
+        torch.cuda.synchronize()
+        return l0.elapsed_time(l1) / nsets
+
     for i in range(warmup):
         one(i)
     torch.cuda.synchronize()
+    link_before = copies_only()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(s_in)
     s_comp.wait_stream(s_in)
@@ -280,25 +306,9 @@ def run_e2e(wl, steps, warmup):
     for w in sets:
         w.check_status()
     e2e_ms = start.elapsed_time(end) / steps
-    # The same copies with no compute, both directions at once: what this
-    # box's host link allows per step right now (the e2e bound).
-    l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    l0.record(s_in)
-    s_out.wait_stream(s_in)
-    for r in range(nsets):                 # every buffer set once, as the loop uses them
-        w = sets[r]
-        with torch.cuda.stream(s_in):
-            for k, dst in ins(w).items():
-                dst.copy_(pinned_in[k], non_blocking=True)
-        with torch.cuda.stream(s_out):
-            for o, p in zip(outs(w), pinned_out[r]):
-                p.copy_(o, non_blocking=True)
-    s_in.wait_stream(s_out)
-    l1.record(s_in)
-    torch.cuda.synchronize()
-    link_ms = l0.elapsed_time(l1) / nsets
+    link_after = copies_only()
     del sets[1:]
-    return e2e_ms, h2d, d2h, link_ms
+    return e2e_ms, h2d, d2h, (link_before, link_after)
 
 
 def oracle_sample(wl_name, budget_s, seed_rows=None):
@@ -368,109 +378,146 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-def run_full_schedule(args):
+def full_schedule_measure(dev, steps, warmup):
     """The full 32-layer schedule on T=30, H=90, W=160 (N=432000): layer l
     runs window attention in the regular layout if l is even, else shifted;
-    between layers the packed qkv rows [N, 3, 24, 128] bf16 are re-laid out
-    into the next layer's order (31 transitions); the text output of every
-    layer is mean-reduced.  One step = all 32 layers."""
+    the text output of every layer is mean-reduced.  Three ways to bring the
+    rows into the next layer's order between layers (31 transitions), each
+    timed as its own 32-layer step:
+
+      qkv      attention (video output in canonical order), then the packed
+               q/k/v rows [N, 3, 24, 128] bf16 re-laid out into the next
+               layer's order (wp_permute);
+      unfused  attention (canonical output), then the video output
+               [N, 24, 128] re-laid out canonical -> next layout (wp_permute);
+      fused    attention writing its video output straight into the next
+               layer's order (wp_window_attn_to): no separate pass.
+
+    In the last two the next layer reads q/k/v already in its own order (a
+    model's projections after the attention output would produce them
+    there).  Returns a dict of the three measurements."""
     import video_dit_shifted_gb300 as vds
     from video_dit_shifted_gb300 import schedule, synth
-    import __graft_entry__
-    __graft_entry__.build()
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
     T, H, W, heads, hd, L = 30, 90, 160, 24, 128, 256
     plan = vds.Plan(T, H, W, 4, 3, 3, device=dev)
     N = plan.N
     layouts = schedule.layer_layouts(32)
     trans = schedule.transitions(layouts)
     x = synth.attention_inputs(N, L, heads, hd, torch.bfloat16, dev)
-    bufs = [x["vid_buf"], torch.empty_like(x["vid_buf"])]      # ping-pong, starts in REGULAR order
+    qkv = {vds.REGULAR: x["vid_buf"], vds.SHIFTED: torch.empty_like(x["vid_buf"])}
+    vds.permute(plan, qkv[vds.REGULAR].view(N, -1), qkv[vds.SHIFTED].view(N, -1), vds.REGULAR, vds.SHIFTED)
+    ping = [x["vid_buf"], torch.empty_like(x["vid_buf"])]      # qkv variant: starts in REGULAR order
     txt = x["txt_buf"]
-    o_vid = torch.empty((N, heads, hd), dtype=torch.bfloat16, device=dev)
+    o_vid = [torch.empty((N, heads, hd), dtype=torch.bfloat16, device=dev) for _ in range(2)]
     o_txt = torch.empty((32, L, heads, hd), dtype=torch.bfloat16, device=dev)
     ws = {l: vds.make_workspace(plan, l, heads, hd, L, vds.BF16, dev) for l in (vds.REGULAR, vds.SHIFTED)}
     flops = {l: attn_flops(np.diff(plan.host_tables(l)[0]), heads, hd, L) for l in (vds.REGULAR, vds.SHIFTED)}
     step_flops = sum(flops[l] for l in layouts)
-    row_B = bufs[0][0].numel() * 2
-    step_bytes = len(trans) * 2.0 * N * row_B
+    qkv_row_B = x["vid_buf"][0].numel() * 2
+    out_row_B = heads * hd * 2
+    ev = lambda: torch.cuda.Event(enable_timing=True)
 
-    def step(ev=None):
+    def step(variant, rec=None):
         cur = 0
         for l, lay in enumerate(layouts):
-            b = bufs[cur]
-            if ev: ev[0].record()
-            vds.window_attn(plan, lay, b[:, 0], b[:, 1], b[:, 2], txt[:, 0], txt[:, 1], txt[:, 2], o_vid,
-                            o_txt[l], ws[lay])
-            if ev: ev[1].record(); ev[2].append((ev[0], ev[1]))
-            if l + 1 < len(layouts):
-                nxt = layouts[l + 1]
-                if ev: ev[3].record()
-                vds.permute(plan, bufs[cur].view(N, -1), bufs[1 - cur].view(N, -1), lay, nxt)
-                if ev: ev[4].record(); ev[5].append((ev[3], ev[4]))
-                cur = 1 - cur
-                if ev:
-                    ev[0], ev[1], ev[3], ev[4] = (torch.cuda.Event(enable_timing=True) for _ in range(4))
+            nxt = layouts[l + 1] if l + 1 < len(layouts) else None
+            b = ping[cur] if variant == "qkv" else qkv[lay]
+            a0, a1 = ev(), ev()
+            a0.record()
+            out_layout = nxt if (variant == "fused" and nxt is not None) else vds.CANONICAL
+            vds.window_attn(plan, lay, b[:, 0], b[:, 1], b[:, 2], txt[:, 0], txt[:, 1], txt[:, 2], o_vid[0],
+                            o_txt[l], ws[lay], out_layout=out_layout)
+            a1.record()
+            p = None
+            if nxt is not None and variant != "fused":
+                p0, p1 = ev(), ev()
+                p0.record()
+                if variant == "qkv":
+                    vds.permute(plan, ping[cur].view(N, -1), ping[1 - cur].view(N, -1), lay, nxt)
+                    cur = 1 - cur
+                else:
+                    vds.permute(plan, o_vid[0].view(N, -1), o_vid[1].view(N, -1), vds.CANONICAL, nxt)
+                p1.record()
+                p = (p0, p1)
+            if rec is not None:
+                rec.append(((a0, a1), p))
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    for l, w in ws.items():
-        assert vds.read_status(w) == 0
+    out = {}
+    for variant in ("qkv", "unfused", "fused"):
+        for _ in range(warmup):
+            step(variant)
+        torch.cuda.synchronize()
+        for l, w in ws.items():
+            if vds.read_status(w) != 0:
+                raise RuntimeError("device status set in the full schedule (%s)" % variant)
+        s, e = ev(), ev()
+        rec = []
+        s.record()
+        for _ in range(steps):
+            step(variant, rec)
+        e.record()
+        torch.cuda.synchronize()
+        ms = s.elapsed_time(e) / steps
+        attn_ms = sum(a[0].elapsed_time(a[1]) for a, _ in rec) / steps
+        perm = [p[0].elapsed_time(p[1]) for _, p in rec if p is not None]
+        perm_ms = sum(perm) / steps
+        row_B = {"qkv": qkv_row_B, "unfused": out_row_B, "fused": 0}[variant]
+        perm_bytes = len(trans) * 2.0 * N * row_B
+        out[variant] = {"ms_per_step": ms, "tflops": step_flops / (ms * 1e-3) / 1e12,
+                        "attn_ms_per_step": attn_ms, "attn_tflops": step_flops / (attn_ms * 1e-3) / 1e12,
+                        "relayout_ms_per_step": perm_ms, "relayout_gb_per_step": perm_bytes / 1e9,
+                        "relayout_gbs": (perm_bytes / (perm_ms * 1e-3) / 1e9) if perm_ms > 0 else None,
+                        "gpu_launches_per_step": 2 * len(layouts) + (len(trans) if variant != "fused" else 0)}
+    out["attn_tflop_per_step"] = step_flops / 1e12
+    out["fused_saves"] = {"ms_per_step": out["unfused"]["ms_per_step"] - out["fused"]["ms_per_step"],
+                          "gb_per_step": out["unfused"]["relayout_gb_per_step"]}
+    plan.close()
+    del x, qkv, ping, o_vid, o_txt, ws
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_full_schedule(args):
+    """--workload full: the 32-layer schedule (see full_schedule_measure) as
+    its own JSON line; value = attention TFLOP of a step / step time of the
+    qkv variant."""
+    import __graft_entry__
+    __graft_entry__.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
     clocks = ClockSampler(0)
     clocks.start()
-    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    attn_pairs, perm_pairs = [], []
-    s.record()
-    for _ in range(args.steps):
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)] + [attn_pairs] + \
-             [torch.cuda.Event(enable_timing=True) for _ in range(2)] + [perm_pairs]
-        step(ev)
-    e.record()
-    torch.cuda.synchronize()
+    r = full_schedule_measure(dev, args.steps, args.warmup)
     clk = clocks.stop()
-    ms = s.elapsed_time(e) / args.steps
-    attn_ms = sum(a.elapsed_time(b) for a, b in attn_pairs) / args.steps
-    perm_ms = sum(a.elapsed_time(b) for a, b in perm_pairs) / args.steps
     peaks, peak_src = load_peaks()
-    a_tf = step_flops / (attn_ms * 1e-3) / 1e12
-    gbs = step_bytes / (perm_ms * 1e-3) / 1e9
-    line = {"metric": METRIC, "value": step_flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "n_gpus": 1,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+    q = r["qkv"]
+    line = {"metric": METRIC, "value": q["tflops"], "unit": "TFLOP/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": q["ms_per_step"], "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": "full schedule: 32 alternating regular/shifted layers (31 re-layouts of packed "
                                    "qkv [N,3,24,128] bf16) on T=30 H=90 W=160 (N=432000), nt=4 nh=3 nw=3, "
                                    "heads=24 head_dim=128, text L=256, text mean per layer",
                        "l2": "inputs larger than L2: no flush"},
-            "attn_tflops": a_tf, "attn_frac_bf16_peak": a_tf / peaks["bf16_tflops"],
-            "attn_ms_per_step": attn_ms, "attn_tflop_per_step": step_flops / 1e12,
-            "relayout_gbs": gbs, "relayout_frac_hbm": gbs / peaks["hbm_gbs"], "relayout_ms_per_step": perm_ms,
-            "relayout_gb_per_step": step_bytes / 1e9, "peak_source": peak_src,
-            "gpu_launches": args.steps * (2 * len(layouts) + len(trans)), "clocks": clk}
+            "attn_tflops": q["attn_tflops"], "attn_frac_bf16_peak": q["attn_tflops"] / peaks["bf16_tflops"],
+            "relayout_gbs": q["relayout_gbs"], "relayout_frac_hbm": q["relayout_gbs"] / peaks["hbm_gbs"],
+            "variants": r, "peak_source": peak_src,
+            "gpu_launches": args.steps * q["gpu_launches_per_step"], "clocks": clk}
     print(json.dumps(line), flush=True)
-    plan.close()
 
 
-def run_sweep(args):
+def sweep_measure(dev, steps, warmup):
     """The re-layout sweep: hidden rows [N, 2560] bf16 permuted regular ->
     shifted and back on grids 45x80 / 68x120 / 90x160 x T in {5, 21, 30}
     (nt, nh, nw = 4, 3, 3).  Each timed launch follows an L2 flush (a write
     of twice the L2 size); points whose footprint is under four times L2 are
-    flagged.  Bytes = 2 * N * 5120 per launch (the 4-byte table read per
-    row is not counted).  Prints one JSON line."""
+    flagged and left out of the median.  Bytes = 2 * N * 5120 per launch (the
+    4-byte table read per row is not counted)."""
     import video_dit_shifted_gb300 as vds
     from video_dit_shifted_gb300 import synth
-    import __graft_entry__
-    __graft_entry__.build()
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
     peaks, peak_src = load_peaks()
     points = []
-    clocks = ClockSampler(0)
-    clocks.start()
     for (H, W) in ((45, 80), (68, 120), (90, 160)):
         for T in (5, 21, 30):
             plan = vds.Plan(T, H, W, 4, 3, 3, device=dev)
@@ -482,10 +529,10 @@ def run_sweep(args):
             res = {}
             for name, a, b, (x, y) in (("regular->shifted", vds.REGULAR, vds.SHIFTED, (src, dst)),
                                        ("shifted->regular", vds.SHIFTED, vds.REGULAR, (dst, back))):
-                for _ in range(args.warmup):
+                for _ in range(warmup):
                     vds.permute(plan, x, y, a, b)
                 ms = []
-                for _ in range(args.steps):
+                for _ in range(steps):
                     flush.fill_(1)
                     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                     e0.record()
@@ -502,20 +549,66 @@ def run_sweep(args):
                            "near_l2": nbytes < 4 * l2, **res})
             plan.close()
             del src, dst, back
-    clk = clocks.stop()
+    del flush
+    torch.cuda.empty_cache()
     big = [p for p in points if not p["near_l2"]]
     gbs = [p[d]["gbs"] for p in big for d in ("regular->shifted", "shifted->regular")]
-    line = {"metric": "re-layout GB/s (% HBM), [N,2560] bf16 sweep", "value": statistics.median(gbs),
+    med = statistics.median(gbs)
+    return {"median_gbs": med, "frac": med / peaks["hbm_gbs"], "peak": peaks["hbm_gbs"], "peak_source": peak_src,
+            "min_gbs": min(gbs), "max_gbs": max(gbs), "points_in_median": 2 * len(big), "points": points,
+            "l2": "L2 flushed (write of %d MB) before every timed launch" % (2 * l2 // 2**20),
+            "gpu_launches": len(points) * 2 * steps}
+
+
+def run_sweep(args):
+    """--workload sweep: the re-layout sweep (see sweep_measure) as its own
+    JSON line."""
+    import __graft_entry__
+    __graft_entry__.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    clocks = ClockSampler(0)
+    clocks.start()
+    r = sweep_measure(dev, args.steps, args.warmup)
+    clk = clocks.stop()
+    line = {"metric": "re-layout GB/s (% HBM), [N,2560] bf16 sweep", "value": r["median_gbs"],
             "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
             "config": {"workload": "re-layout sweep: hidden rows [N,2560] bf16, grids 45x80/68x120/90x160 x "
                                    "T in {5,21,30}, nt nh nw = 4 3 3, both directions; value = median GB/s "
                                    "over the points above 4x L2",
-                       "l2": "L2 flushed (write of %d MB) before every timed launch" % (2 * l2 // 2**20)},
-            "peak": peaks["hbm_gbs"], "peak_source": peak_src, "frac": statistics.median(gbs) / peaks["hbm_gbs"],
-            "points": points, "gpu_launches": len(points) * 2 * args.steps, "clocks": clk}
+                       "l2": r["l2"]},
+            "peak": r["peak"], "peak_source": r["peak_source"], "frac": r["frac"],
+            "points": r["points"], "gpu_launches": r["gpu_launches"], "clocks": clk}
     print(json.dumps(line), flush=True)
+
+
+def layer_measure(name, dev, reps, warmup):
+    """Both attention layers of a workload timed alone (wp_window_attn:
+    tcgen05 kernel + text mean), `reps` launches each after `warmup`;
+    inputs larger than L2.  Returns per-layout ms and TFLOP/s."""
+    import video_dit_shifted_gb300 as vds
+    wl = Workload(name, dev, hidden=False)
+    peaks, _ = load_peaks()
+    out = {}
+    for layout, lname in ((vds.REGULAR, "regular"), (vds.SHIFTED, "shifted")):
+        for _ in range(warmup):
+            wl.attn(layout)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            wl.attn(layout)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        tf = wl.flops[layout] / (ms * 1e-3) / 1e12
+        out[lname] = {"ms": ms, "tflops": tf, "frac_bf16_peak": tf / peaks["bf16_tflops"],
+                      "tflop_per_launch": wl.flops[layout] / 1e12}
+    wl.check_status()
+    del wl
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_ours(args):
@@ -575,7 +668,8 @@ def run_ours(args):
     e2e = {"value": world * step_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
            "steps": args.e2e_steps,
-           "copies_only_ms_per_step": link_ms,
+           "copies_only_ms_per_step": min(link_ms),
+           "copies_only_ms_before_after": list(link_ms),
            "pipelining": "copy-in of step i+1 and copy-out of step i-1 overlap step i (3 device buffer sets, "
                          "3 streams); every step's copies are inside the timed region"}
     # Window-local RoPE of q and k (a separate in-place pass, not part of the
@@ -617,6 +711,30 @@ def run_ours(args):
                   "ms_fused": fused_ms, "tflops_fused": f_reg / (fused_ms * 1e-3) / 1e12,
                   "ms_rope_then_attn": rope_ms + attn_reg_ms, "ms_attn": attn_reg_ms, "ms_rope": rope_ms}
     del ws_rope
+    # The metric's other grid and the other configurations, measured in the
+    # same run (single-GPU runs only; each after its own warm-up).
+    extras = None
+    if world == 1 and not args.no_extras:
+        torch.cuda.empty_cache()
+        xclk = ClockSampler(dev.index)
+        xclk.start()
+        sw = sweep_measure(dev, steps=5, warmup=3)
+        extras = {
+            "attn_720p": layer_measure("720p", dev, reps=20, warmup=3),
+            "relayout_sweep": {k: sw[k] for k in ("median_gbs", "frac", "min_gbs", "max_gbs", "points_in_median",
+                                                  "peak", "l2")},
+            "full_schedule": full_schedule_measure(dev, steps=2, warmup=3),
+        }
+        extras["relayout_sweep"]["workload"] = ("[N,2560] bf16 rows, regular->shifted and back, grids 45x80/68x120/"
+                                                "90x160 x T in {5,21,30}; median of 5 launches per point, L2 flushed "
+                                                "before each; median over the points above 4x L2")
+        extras["relayout_sweep"]["points_gbs"] = {p["grid"]: [round(p[d]["gbs"], 1) for d in
+                                                              ("regular->shifted", "shifted->regular")]
+                                                  for p in sw["points"]}
+        extras["full_schedule"]["workload"] = ("32 alternating layers on T=30 H=90 W=160 (N=432000), 24x128 heads, "
+                                               "L=256; 2 steps after 3 per variant (see bench.py "
+                                               "full_schedule_measure)")
+        extras["clocks"] = xclk.stop()
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tf, pairs, fl, secs = oracle_sample(args.workload, args.cpu_budget_s)
@@ -636,9 +754,21 @@ def run_ours(args):
                 "rope_fused": rope_fused,
                 "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": wl.launches_per_step * args.steps, "clocks": clk}
+        if extras is not None:
+            line.update(extras_line(extras))
         print(json.dumps(line), flush=True)
     if pg is not None:
         pg.destroy_process_group()
+
+
+def extras_line(x):
+    """Keys the default line carries for the other configurations."""
+    fs = x["full_schedule"]
+    return {"attn_720p": x["attn_720p"], "relayout_sweep": x["relayout_sweep"],
+            "full_schedule": {"workload": fs["workload"], "attn_tflop_per_step": fs["attn_tflop_per_step"],
+                              "qkv": fs["qkv"], "unfused": fs["unfused"], "fused": fs["fused"],
+                              "fused_saves": fs["fused_saves"]},
+            "extras_clocks": x["clocks"]}
 
 
 def main():
@@ -652,6 +782,8 @@ def main():
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--ref-step-s", type=float, default=4.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the 720p layers, the re-layout sweep and the 32-layer schedule")
     args = ap.parse_args()
     if args.warmup < 3:
         print("note: --warmup raised to 3 (timing rules)", file=sys.stderr)
