@@ -711,6 +711,7 @@ def run_ours(args):
                   "ms_fused": fused_ms, "tflops_fused": f_reg / (fused_ms * 1e-3) / 1e12,
                   "ms_rope_then_attn": rope_ms + attn_reg_ms, "ms_attn": attn_reg_ms, "ms_rope": rope_ms}
     del ws_rope
+    fp8 = fp8_measure(wl, attn_reg, attn_shf, args.steps)
     # The metric's other grid and the other configurations, measured in the
     # same run (single-GPU runs only; each after its own warm-up).
     extras = None
@@ -751,7 +752,7 @@ def run_ours(args):
                            "parallelism": "replicas" if world > 1 else "single GPU"},
                 "attn_tflops": attn_tflops, "relayout_gbs": relayout_gbs,
                 "roofline": roofline, "roofline_relayout": relayout, "roofline_rope": rope,
-                "rope_fused": rope_fused,
+                "rope_fused": rope_fused, "fp8_qk": fp8,
                 "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": wl.launches_per_step * args.steps, "clocks": clk}
         if extras is not None:
@@ -759,6 +760,58 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
     if pg is not None:
         pg.destroy_process_group()
+
+
+def fp8_measure(wl, attn_reg, attn_shf, steps):
+    """Both 1080p layers with e4m3 q/k (wp_window_attn_fp8) against the bf16
+    call of the timed steps, and the quantise pass (wp_quantize_e4m3 of q and
+    k, HBM-bound) that a caller without e4m3 projections would add."""
+    vds = wl.vds
+    N, heads, hd, L = wl.N, wl.w["heads"], wl.w["hd"], wl.w["L"]
+    inv = 64.0
+    qk8 = {l: torch.empty((N, 2, heads, hd), dtype=torch.uint8, device=wl.dev) for l in (vds.REGULAR, vds.SHIFTED)}
+    qkt8 = torch.empty((L, 2, heads, hd), dtype=torch.uint8, device=wl.dev)
+
+    def quantize(l):
+        b = wl.qkv[l]
+        for i in range(2):
+            vds.quantize_e4m3(b[:, i].reshape(N, heads * hd), qk8[l][:, i].reshape(N, heads * hd), inv)
+
+    for i in range(2):
+        vds.quantize_e4m3(wl.txt[:, i].reshape(L, heads * hd), qkt8[:, i].reshape(L, heads * hd), inv)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for l in (vds.REGULAR, vds.SHIFTED):
+        quantize(l)
+    e0.record()
+    for _ in range(5):
+        quantize(vds.REGULAR)
+    e1.record()
+    torch.cuda.synchronize()
+    q_ms = e0.elapsed_time(e1) / 5
+    q_bytes = 2 * N * heads * hd * (2 + 1)
+    out = {"kernel": "attn_tc_kernel<128, e4m3 Q K^T> (wp_window_attn_fp8), q/k codes = e4m3(x * 64)",
+           "quantize_ms": q_ms, "quantize_gbs": q_bytes / (q_ms * 1e-3) / 1e9,
+           "quantize_bytes": q_bytes}
+    t = wl.txt
+    for l, name, bf in ((vds.REGULAR, "regular", attn_reg), (vds.SHIFTED, "shifted", attn_shf)):
+        run = lambda: vds.window_attn_fp8(wl.plan, l, qk8[l][:, 0], qk8[l][:, 1], wl.qkv[l][:, 2], qkt8[:, 0],
+                                          qkt8[:, 1], t[:, 2], 1.0 / inv, 1.0 / inv, wl.o_vid[l], wl.o_txt[l],
+                                          wl.ws[l])
+        for _ in range(3):
+            run()
+        e0.record()
+        for _ in range(10):
+            run()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / 10
+        if vds.read_status(wl.ws[l]) != 0:
+            raise RuntimeError("device status set by wp_window_attn_fp8")
+        bf_ms = sum(bf) / steps
+        out[name] = {"ms": ms, "tflops": wl.flops[l] / (ms * 1e-3) / 1e12, "ms_bf16": bf_ms,
+                     "speedup_vs_bf16": bf_ms / ms}
+    del qk8, qkt8
+    return out
 
 
 def extras_line(x):

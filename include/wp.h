@@ -266,6 +266,48 @@ int wp_window_attn_rope(const wp_plan* plan, int layout, int out_layout, int hea
                         size_t ws_bytes, float softmax_scale, float rope_base,
                         void* stream);
 
+/* wp_window_attn_fp8 -- wp_window_attn_to with Q K^T on e4m3 operands
+ * (tcgen05 kind::f8f6f4, twice the bf16 rate per instruction); P V, the
+ * softmax, the outputs and the text mean as in the bf16 call.  The pages
+ * mention low-precision training only as context ("Scaling Video Training
+ * with Parallelism", §Key claims: NVFP4 for LongLive-2.0) and define no such
+ * path; this is an opt-in variant for callers whose q/k projection already
+ * emits e4m3, with per-tensor scales:
+ *     scores = (q8 * q_scale) . (k8 * k_scale) * softmax_scale
+ * (softmax_scale <= 0: 1/sqrt(head_dim)).  Its error against exact attention
+ * on the unquantised q/k is that of e4m3 rounding (3 mantissa bits) and is
+ * larger than the bf16 call's.
+ * Layout: q8, k8 [N, heads, 128] one byte per element (e4m3 codes, layout
+ * `layout` order, shared row stride qk_row_stride_B); v [N, heads, 128] bf16
+ * (row stride v_row_stride_B); qt8, kt8 [L, heads, 128] e4m3 (stride
+ * txt_qk_row_stride_B); vt [L, heads, 128] bf16 (stride txt_v_row_stride_B);
+ * o_vid, o_txt, workspace (wp_attn_workspace_bytes with WP_BF16) as in
+ * wp_window_attn_to.
+ * Supported (WP_EUNSUPPORTED otherwise): head_dim 128; pointers and strides
+ * multiples of 16 bytes, each stride at least one row.  WP_EINVAL: scales
+ * not finite and > 0, and the wp_window_attn_to cases. */
+int wp_window_attn_fp8(const wp_plan* plan, int layout, int out_layout, int heads,
+                       int head_dim, int L, const void* q8, const void* k8,
+                       int64_t qk_row_stride_B, const void* v, int64_t v_row_stride_B,
+                       const void* qt8, const void* kt8, int64_t txt_qk_row_stride_B,
+                       const void* vt, int64_t txt_v_row_stride_B, float q_scale,
+                       float k_scale, void* o_vid, int64_t o_vid_row_stride_B,
+                       void* o_txt, void* workspace, size_t ws_bytes,
+                       float softmax_scale, void* stream);
+
+/* wp_quantize_e4m3 -- bf16 rows to e4m3 codes for wp_window_attn_fp8:
+ *     code = e4m3(fp32(x) * inv_scale)
+ * one fp32 multiply (round to nearest even), then the nearest e4m3 value
+ * (ties to even), saturated to +-448; dequantised value = code / inv_scale
+ * (pass q_scale = 1 / inv_scale to the attention call; a power of two keeps
+ * that exact).  src [rows, cols] bf16 with row stride src_row_stride_B; dst
+ * [rows, cols] bytes with row stride dst_row_stride_B.  WP_EUNSUPPORTED:
+ * cols not a multiple of 16, pointers or strides not 16-byte aligned, or a
+ * stride shorter than a row.  WP_EINVAL: NULL pointers, negative sizes,
+ * inv_scale not finite and > 0.  Asynchronous on `stream`. */
+int wp_quantize_e4m3(const void* src, int64_t rows, int cols, int64_t src_row_stride_B,
+                     void* dst, int64_t dst_row_stride_B, float inv_scale, void* stream);
+
 /* wp_window_attn_static -- wp_window_attn for callers that cannot allocate
  * device memory when they run attention (a runtime that owns a fixed memory
  * pool and forbids allocation from plugins, a latency-bound loop that cannot

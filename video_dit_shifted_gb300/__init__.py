@@ -8,5 +8,5 @@ runs in libwp.so (include/wp.h); ``wp`` is its ctypes binding.
 """
 from . import wp  # noqa: F401
 from .wp import (BF16, CANONICAL, FP32, REGULAR, SHIFTED, Plan, debug_stall_next,  # noqa: F401
-                 make_workspace, permute, read_status, rope, rope_workspace_bytes, window_attn,
-                 window_attn_rope, workspace_bytes)
+                 make_workspace, permute, quantize_e4m3, read_status, rope, rope_workspace_bytes, window_attn,
+                 window_attn_fp8, window_attn_rope, workspace_bytes)

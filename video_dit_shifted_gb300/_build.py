@@ -17,7 +17,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libwp.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["plan.cpp", "permute.cu", "attn.cu", "attn_tc.cu", "attn_static.cu", "rope.cu"]
+SOURCES = ["plan.cpp", "permute.cu", "attn.cu", "attn_tc.cu", "attn_static.cu", "rope.cu", "fp8.cu"]
 
 
 def _nvcc():

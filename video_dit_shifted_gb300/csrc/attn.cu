@@ -233,6 +233,33 @@ extern "C" int wp_attn_rope_workspace_bytes(const wp_plan* plan, int layout, int
 
 namespace {
 
+// The plan's tables for one call: windows of `layout`, and the output row
+// of every input row for `out_layout`.
+int set_tables(AttnCall& c, const wp_plan* plan, int layout, int out_layout, int L) {
+  const LayoutTables& LT = plan->lay[layout];
+  c.N = plan->N;
+  c.nwin = LT.nwin;
+  c.max_tokens = LT.max_tokens;
+  c.win_off = dev_ptr<int32_t>(plan, plan->dlay[layout].win_off);
+  // Row of the output layout for each row of the input layout:
+  // canonical -> ids; the same layout -> identity (no table); another window
+  // layout b -> pos_b[ids_layout[q]], which is the fused table perm[b -> layout].
+  if (out_layout == WP_CANONICAL)
+    c.ids = dev_ptr<int32_t>(plan, plan->dlay[layout].ids);
+  else if (out_layout == layout)
+    c.ids = nullptr;
+  else
+    c.ids = dev_ptr<int32_t>(plan, plan->perm_off[out_layout][layout]);
+  c.pair_off[0] = dev_ptr<int32_t>(plan, plan->dlay[layout].pair_off[0]);
+  c.pair_off[1] = dev_ptr<int32_t>(plan, plan->dlay[layout].pair_off[1]);
+  c.text_tiles = (L + kTileM - 1) / kTileM;
+  const int64_t pairs = static_cast<int64_t>(LT.pair_off[c.text_tiles & 1][LT.nwin]) +
+                        static_cast<int64_t>(LT.nwin) * (c.text_tiles >> 1);
+  if (pairs > 0x7fffffff) return fail(WP_EUNSUPPORTED, "too many query tiles");
+  c.total_pairs = static_cast<int>(pairs);
+  return WP_OK;
+}
+
 int window_attn_impl(const wp_plan* plan, int layout, int out_layout, int heads, int head_dim, int L,
                      int dtype, const void* q, const void* k, const void* v, int64_t vid_row_stride_B,
                      const void* qt, const void* kt, const void* vt, int64_t txt_row_stride_B,
@@ -266,29 +293,16 @@ int window_attn_impl(const wp_plan* plan, int layout, int out_layout, int heads,
   if (ws_bytes < need) return fail(WP_EINVAL, "workspace too small: %zu < %zu bytes", ws_bytes, need);
   if (int rc = require_uploaded(plan)) return rc;
 
-  const LayoutTables& LT = plan->lay[layout];
   AttnCall c{};
   c.layout = layout; c.heads = heads; c.hd = head_dim; c.L = L; c.dtype = dtype;
-  c.q = q; c.k = k; c.v = v; c.vid_stride_B = vid_row_stride_B;
+  c.q = q; c.k = k; c.v = v; c.vid_stride_B = vid_row_stride_B; c.vid_v_stride_B = vid_row_stride_B;
   c.qt = qt; c.kt = kt; c.vt = vt; c.txt_stride_B = txt_row_stride_B; c.vt_stride_B = txt_row_stride_B;
   c.o_vid = o_vid; c.o_stride_B = o_vid_row_stride_B; c.o_txt = o_txt;
   c.status = static_cast<int*>(workspace);
   c.partial = reinterpret_cast<float*>(static_cast<char*>(workspace) + kStatusBytes);
   c.scale = softmax_scale > 0.f ? softmax_scale : 1.f / std::sqrt(static_cast<float>(head_dim));
   c.stream = static_cast<cudaStream_t>(stream);
-  c.N = plan->N;
-  c.nwin = LT.nwin;
-  c.max_tokens = LT.max_tokens;
-  c.win_off = dev_ptr<int32_t>(plan, plan->dlay[layout].win_off);
-  // Row of the output layout for each row of the input layout:
-  // canonical -> ids; the same layout -> identity (no table); another window
-  // layout b -> pos_b[ids_layout[q]], which is the fused table perm[b -> layout].
-  if (out_layout == WP_CANONICAL)
-    c.ids = dev_ptr<int32_t>(plan, plan->dlay[layout].ids);
-  else if (out_layout == layout)
-    c.ids = nullptr;
-  else
-    c.ids = dev_ptr<int32_t>(plan, plan->perm_off[out_layout][layout]);
+  if (int rc = set_tables(c, plan, layout, out_layout, L)) return rc;
   if (rope) {
     c.rope = true;
     c.boxes = dev_ptr<int32_t>(plan, plan->dlay[layout].boxes);
@@ -297,13 +311,6 @@ int window_attn_impl(const wp_plan* plan, int layout, int out_layout, int heads,
     c.ww = plan->ww;
     rope_theta(rope_base, c.rope_theta);
   }
-  c.pair_off[0] = dev_ptr<int32_t>(plan, plan->dlay[layout].pair_off[0]);
-  c.pair_off[1] = dev_ptr<int32_t>(plan, plan->dlay[layout].pair_off[1]);
-  c.text_tiles = (L + kTileM - 1) / kTileM;
-  const int64_t pairs = static_cast<int64_t>(LT.pair_off[c.text_tiles & 1][LT.nwin]) +
-                        static_cast<int64_t>(LT.nwin) * (c.text_tiles >> 1);
-  if (pairs > 0x7fffffff) return fail(WP_EUNSUPPORTED, "too many query tiles");
-  c.total_pairs = static_cast<int>(pairs);
 
   if (int rc = cuda_check(cudaMemsetAsync(workspace, 0, kStatusBytes, c.stream), "cudaMemsetAsync(status)"))
     return rc;
@@ -359,6 +366,56 @@ extern "C" int wp_window_attn_rope(const wp_plan* plan, int layout, int out_layo
   return window_attn_impl(plan, layout, out_layout, heads, head_dim, L, dtype, q, k, v, vid_row_stride_B,
                           qt, kt, vt, txt_row_stride_B, o_vid, o_vid_row_stride_B, o_txt, workspace,
                           ws_bytes, softmax_scale, stream, rope_base);
+}
+
+extern "C" int wp_window_attn_fp8(const wp_plan* plan, int layout, int out_layout, int heads, int head_dim,
+                                  int L, const void* q8, const void* k8, int64_t qk_row_stride_B, const void* v,
+                                  int64_t v_row_stride_B, const void* qt8, const void* kt8,
+                                  int64_t txt_qk_row_stride_B, const void* vt, int64_t txt_v_row_stride_B,
+                                  float q_scale, float k_scale, void* o_vid, int64_t o_vid_row_stride_B,
+                                  void* o_txt, void* workspace, size_t ws_bytes, float softmax_scale,
+                                  void* stream) {
+  if (int rc = check_shape(plan, layout, heads, head_dim, L, WP_BF16)) return rc;
+  if (head_dim != 128) return fail(WP_EUNSUPPORTED, "e4m3 attention supports head_dim 128 (got %d)", head_dim);
+  if (out_layout < 0 || out_layout >= kNumLayouts) return fail(WP_EINVAL, "bad output layout %d", out_layout);
+  if (!(q_scale > 0.f) || !(k_scale > 0.f) || !std::isfinite(q_scale) || !std::isfinite(k_scale))
+    return fail(WP_EINVAL, "q_scale and k_scale must be finite and > 0");
+  if (!q8 || !k8 || !v || !o_vid || !workspace) return fail(WP_EINVAL, "q8, k8, v, o_vid or workspace is NULL");
+  if (L > 0 && (!qt8 || !kt8 || !vt || !o_txt)) return fail(WP_EINVAL, "text pointers are NULL with L=%d", L);
+  for (const void* ptr : {q8, k8, v, static_cast<const void*>(o_vid), static_cast<const void*>(workspace)})
+    if (!aligned16(ptr)) return fail(WP_EUNSUPPORTED, "q8/k8/v/o_vid/workspace must be 16-byte aligned");
+  if (L > 0)
+    for (const void* ptr : {qt8, kt8, vt, static_cast<const void*>(o_txt)})
+      if (!aligned16(ptr)) return fail(WP_EUNSUPPORTED, "qt8/kt8/vt/o_txt must be 16-byte aligned");
+  const int64_t qk_B = static_cast<int64_t>(heads) * head_dim, bf_B = 2 * qk_B;
+  auto ok_stride = [](int64_t s, int64_t min_B) { return s >= min_B && (s & 15) == 0; };
+  if (!ok_stride(qk_row_stride_B, qk_B) || !ok_stride(v_row_stride_B, bf_B) || !ok_stride(o_vid_row_stride_B, bf_B) ||
+      (L > 0 && (!ok_stride(txt_qk_row_stride_B, qk_B) || !ok_stride(txt_v_row_stride_B, bf_B))))
+    return fail(WP_EUNSUPPORTED, "row strides must be multiples of 16 and hold a row (q/k %lld B, v/out %lld B)",
+                (long long)qk_B, (long long)bf_B);
+  size_t need = 0;
+  workspace_bytes(plan, layout, heads, head_dim, L, &need);
+  if (ws_bytes < need) return fail(WP_EINVAL, "workspace too small: %zu < %zu bytes", ws_bytes, need);
+  if (int rc = require_uploaded(plan)) return rc;
+
+  AttnCall c{};
+  c.layout = layout; c.heads = heads; c.hd = head_dim; c.L = L; c.dtype = WP_BF16;
+  c.fp8 = true;
+  c.q = q8; c.k = k8; c.v = v; c.vid_stride_B = qk_row_stride_B; c.vid_v_stride_B = v_row_stride_B;
+  c.qt = qt8; c.kt = kt8; c.vt = vt; c.txt_stride_B = txt_qk_row_stride_B; c.vt_stride_B = txt_v_row_stride_B;
+  c.o_vid = o_vid; c.o_stride_B = o_vid_row_stride_B; c.o_txt = o_txt;
+  c.status = static_cast<int*>(workspace);
+  c.partial = reinterpret_cast<float*>(static_cast<char*>(workspace) + kStatusBytes);
+  // scores = (q8 * q_scale) . (k8 * k_scale) * softmax_scale
+  c.scale = (softmax_scale > 0.f ? softmax_scale : 1.f / std::sqrt(static_cast<float>(head_dim))) * q_scale * k_scale;
+  c.stream = static_cast<cudaStream_t>(stream);
+  if (int rc = set_tables(c, plan, layout, out_layout, L)) return rc;
+  if (int rc = cuda_check(cudaMemsetAsync(workspace, 0, kStatusBytes, c.stream), "cudaMemsetAsync(status)"))
+    return rc;
+  if (int rc = launch_attn_bf16_tc(c)) return rc;
+  if (L > 0)
+    if (int rc = launch_text_mean(c)) return rc;
+  return ok();
 }
 
 extern "C" int wp_debug_stall_next(int launches) {

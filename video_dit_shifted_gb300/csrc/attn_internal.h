@@ -20,7 +20,8 @@ constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;
 struct AttnCall {
   int layout, heads, hd, L, dtype;
   const void *q, *k, *v;
-  int64_t vid_stride_B;
+  int64_t vid_stride_B;    // q and k
+  int64_t vid_v_stride_B;  // v
   const void *qt, *kt, *vt;
   int64_t txt_stride_B;  // qt and kt
   int64_t vt_stride_B;
@@ -39,6 +40,9 @@ struct AttnCall {
   const int32_t* pair_off[2];  // device
   int total_pairs;             // query-tile pairs over all windows (tile kTileM)
   int text_tiles;              // ceil(L / kTileM)
+  // q, k, qt, kt are e4m3 codes (wp_window_attn_fp8); their dequantisation
+  // scales are folded into `scale`.
+  bool fp8 = false;
   // Window-local RoPE applied inside the kernel (wp_window_attn_rope): the
   // text q/k passed in are already rotated.
   bool rope = false;

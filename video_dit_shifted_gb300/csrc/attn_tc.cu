@@ -85,15 +85,22 @@ constexpr int kMmaWarp = 9;
 constexpr int kTmemCols = 512;
 static_assert(kBM == kTileM, "plan tables count tiles of kTileM rows");
 
-template <int HD>
+// Shared-memory layout.  Q and K are bf16 or, in the e4m3 kernels, one byte
+// per element; V is always bf16.  Every tile is stored as 128-row x 128-byte
+// boxes (128-byte swizzle), one box per 128 bytes of a row.
+template <int HD, bool kFp8 = false>
 struct Cfg {
-  static constexpr int kHalves = HD / 64;          // 64-column (128 B) swizzle blocks
-  static constexpr int kBoxBytes = 128 * 128;      // one 128-row x 128-byte box
-  static constexpr int kTileBytes = kBM * HD * 2;  // a Q, K or V tile
-  static constexpr int kQ = 0;                     // Q tile i at kQ + i*kTileBytes
-  static constexpr int kK = 2 * kTileBytes;        // K stage s at kK + s*kTileBytes
-  static constexpr int kV = 4 * kTileBytes;        // V stage s at kV + s*kTileBytes
-  static constexpr int kBar = 6 * kTileBytes;
+  static constexpr int kHalves = HD / 64;               // V: 64-column (128 B) boxes per row
+  static constexpr int kQKElem = kFp8 ? 1 : 2;          // bytes per Q/K element
+  static constexpr int kQKBoxes = HD * kQKElem / 128;   // Q/K: 128-byte boxes per row
+  static constexpr int kQKBoxCols = 128 / kQKElem;      // Q/K: elements per box row
+  static constexpr int kBoxBytes = 128 * 128;           // one 128-row x 128-byte box
+  static constexpr int kQKTileBytes = kBM * HD * kQKElem;  // a Q or K tile
+  static constexpr int kTileBytes = kBM * HD * 2;       // a V tile
+  static constexpr int kQ = 0;                          // Q tile i at kQ + i*kQKTileBytes
+  static constexpr int kK = 2 * kQKTileBytes;           // K stage s at kK + s*kQKTileBytes
+  static constexpr int kV = 4 * kQKTileBytes;           // V stage s at kV + s*kTileBytes
+  static constexpr int kBar = kV + 2 * kTileBytes;
   static constexpr int kTab = kBar + 256;          // RoPE kernels: cos/sin table
   static constexpr int kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 256 + HD;
 };
@@ -237,6 +244,11 @@ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
+// Instruction descriptor for kind::f8f6f4 with A and B both e4m3 (format
+// code 0 in bits 7-9 and 10-12), both K-major, D fp32.
+constexpr uint32_t idesc_e4m3(int M, int N) {
+  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
 
 // MMA and commit wrappers: called by all 32 lanes of a converged warp; one
 // elected lane issues the instruction.
@@ -244,6 +256,13 @@ __device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint3
   asm volatile(
       "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ss_f8(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
       "l"(a), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }
@@ -456,13 +475,14 @@ __device__ __forceinline__ Item decode_item(const TcParams& p, int it) {
 // that all roles advance identically.
 // 10 warps put 3 warps on one SM sub-partition (16K registers each), which
 // caps a thread at 168 registers.
-template <int HD, bool kRope>
+template <int HD, bool kRope, bool kFp8>
 __global__ void __launch_bounds__(kRope ? kRopeThreads : kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_qt,
                    const __grid_constant__ CUtensorMap tm_kt, const __grid_constant__ CUtensorMap tm_vt,
                    const TcParams p) {
-  using C = Cfg<HD>;
+  static_assert(!(kRope && kFp8), "no RoPE on e4m3 tiles");
+  using C = Cfg<HD, kFp8>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // 1024-aligned for 128 B swizzle
@@ -561,14 +581,14 @@ __global__ void __launch_bounds__(kRope ? kRopeThreads : kThreads, 1)
         const Item x = decode_item(p, it);
         // Q smem is free once the previous item's last Q K^T has completed.
         if (k > 0 && !(good = wait_phase(bq_empty, (k - 1) & 1, abort_flag, p.status))) break;
-        mbar_expect_tx(bq_full, x.nq * C::kTileBytes);
+        mbar_expect_tx(bq_full, x.nq * C::kQKTileBytes);
         for (int i = 0; i < x.nq; ++i) {
           const int t = x.t0 + i;
           const CUtensorMap* map = t < x.vt ? &tm_q : &tm_qt;
           const int row = t < x.vt ? x.a + t * kBM : (t - x.vt) * kBM;
-          for (int hf = 0; hf < C::kHalves; ++hf)
-            tma_load_2d(base + C::kQ + i * C::kTileBytes + hf * C::kBoxBytes, map, bq_full,
-                        x.h * HD + hf * 64, row);
+          for (int hf = 0; hf < C::kQKBoxes; ++hf)
+            tma_load_2d(base + C::kQ + i * C::kQKTileBytes + hf * C::kBoxBytes, map, bq_full,
+                        x.h * HD + hf * C::kQKBoxCols, row);
         }
         ++k;
         auto tile_row = [&](int j) { return j < x.vt ? x.a + j * kBN : (j - x.vt) * kBN; };
@@ -579,15 +599,15 @@ __global__ void __launch_bounds__(kRope ? kRopeThreads : kThreads, 1)
           const int kt = pl;      // K tile of this payload (none when pl == nkv)
           const int vt_ = pl - 1;  // V tile of this payload (none when pl == 0)
           const uint32_t fb = bar(bars->pl_full[slot]);
-          mbar_expect_tx(fb, ((kt < x.nkv) + (vt_ >= 0)) * C::kTileBytes);
+          mbar_expect_tx(fb, (kt < x.nkv ? C::kQKTileBytes : 0) + (vt_ >= 0 ? C::kTileBytes : 0));
           if (vt_ >= 0)
             for (int hf = 0; hf < C::kHalves; ++hf)
               tma_load_2d(base + C::kV + slot * C::kTileBytes + hf * C::kBoxBytes, vt_ < x.vt ? &tm_v : &tm_vt,
                           fb, x.h * HD + hf * 64, tile_row(vt_));
           if (kt < x.nkv)
-            for (int hf = 0; hf < C::kHalves; ++hf)
-              tma_load_2d(base + C::kK + slot * C::kTileBytes + hf * C::kBoxBytes, kt < x.vt ? &tm_k : &tm_kt,
-                          fb, x.h * HD + hf * 64, tile_row(kt));
+            for (int hf = 0; hf < C::kQKBoxes; ++hf)
+              tma_load_2d(base + C::kK + slot * C::kQKTileBytes + hf * C::kBoxBytes, kt < x.vt ? &tm_k : &tm_kt,
+                          fb, x.h * HD + hf * C::kQKBoxCols, tile_row(kt));
         }
       }
       if (*abort_flag) {
@@ -600,19 +620,24 @@ __global__ void __launch_bounds__(kRope ? kRopeThreads : kThreads, 1)
   } else if (warp == kMmaWarp) {
     // ======================= MMA issuer (whole warp, converged) ==========
     {
-      constexpr uint32_t kIdescQK = idesc_bf16(kBM, kBN, false);
+      constexpr uint32_t kIdescQK = kFp8 ? idesc_e4m3(kBM, kBN) : idesc_bf16(kBM, kBN, false);
       constexpr uint32_t kIdescPV = idesc_bf16(kBM, HD, true);
       // Descriptors are built once per tile and advanced by constant offsets
       // (the start-address field holds address >> 4 and never carries out of
       // its 14 bits for a shared-memory address), keeping the issue loop short.
       auto issue_qk = [&](int i, int s) {
         const uint32_t dS = tmem + (i ? C::kColS1 : C::kColS0);
-        const uint64_t qd = sw128_desc(base + C::kQ + i * C::kTileBytes, 16, 1024);
-        const uint64_t kd = sw128_desc(base + C::kK + s * C::kTileBytes, 16, 1024);
+        const uint64_t qd = sw128_desc(base + C::kQ + i * C::kQKTileBytes, 16, 1024);
+        const uint64_t kd = sw128_desc(base + C::kK + s * C::kQKTileBytes, 16, 1024);
+        // one MMA per 32 bytes of the head dimension (16 bf16 or 32 e4m3
+        // elements): 4 per 128-byte box
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {
+        for (int kk = 0; kk < HD * C::kQKElem / 32; ++kk) {
           const uint32_t off16 = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
-          mma_ss(dS, qd + off16, kd + off16, kIdescQK, kk > 0);
+          if constexpr (kFp8)
+            mma_ss_f8(dS, qd + off16, kd + off16, kIdescQK, kk > 0);
+          else
+            mma_ss(dS, qd + off16, kd + off16, kIdescQK, kk > 0);
         }
       };
       auto issue_pv = [&](int i, int s, bool first) {
@@ -739,7 +764,7 @@ __global__ void __launch_bounds__(kRope ? kRopeThreads : kThreads, 1)
       for (int i = 0; i < x.nq; ++i) {
         const int t = x.t0 + i;
         if (t < x.vt)
-          rope_tile(base + C::kQ + i * C::kTileBytes, t * kBM, min(kBM, x.n_w - t * kBM), bh, bw, p.wt, p.wh, tab_s,
+          rope_tile(base + C::kQ + i * C::kQKTileBytes, t * kBM, min(kBM, x.n_w - t * kBM), bh, bw, p.wt, p.wh, tab_s,
                     inv_bhw, inv_bw, rt);
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -748,7 +773,7 @@ __global__ void __launch_bounds__(kRope ? kRopeThreads : kThreads, 1)
         const int slot = e & 1;
         if (!(good = wait_phase(bar(bars->pl_full[slot]), (e >> 1) & 1, abort_flag, p.status))) break;
         if (pl < x.vt)  // this payload's K tile (K_pl) is a video tile
-          rope_tile(base + C::kK + slot * C::kTileBytes, pl * kBN, min(kBN, x.n_w - pl * kBN), bh, bw, p.wt, p.wh, tab_s,
+          rope_tile(base + C::kK + slot * C::kQKTileBytes, pl * kBN, min(kBN, x.n_w - pl * kBN), bh, bw, p.wt, p.wh, tab_s,
                     inv_bhw, inv_bw, rt);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         mbar_arrive(bar(bars->pl_ready[slot]));
@@ -931,33 +956,35 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2D bf16 map over rows x (heads*hd) columns, box 128 rows x 64 columns,
-// 128-byte swizzle; reads past the last row return zeros.
-int make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int64_t stride_B) {
+// 2D map over rows x (heads*hd) columns of bf16 (box 128 rows x 64 columns)
+// or of one-byte e4m3 codes (box 128 rows x 128 columns): 128-byte rows of a
+// box, 128-byte swizzle; reads past the last row return zeros.
+int make_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int64_t stride_B, bool bytes = false) {
   auto fn = encode_fn();
   if (!fn) return fail(WP_ECUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(stride_B)};
-  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t box[2] = {bytes ? 128u : 64u, 128};
   const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+  const CUresult r = fn(m, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                        const_cast<void*>(ptr), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(WP_ECUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
   return WP_OK;
 }
 
-template <int HD, bool kRope>
+template <int HD, bool kRope, bool kFp8>
 int launch(const AttnCall& c) {
   static_assert(!kRope || HD == 128, "the RoPE kernels rotate 128-column heads");
   CUtensorMap mq, mk, mv, mqt, mkt, mvt;
   const int64_t cols = static_cast<int64_t>(c.heads) * HD;
-  if (int rc = make_map(&mq, c.q, c.N, cols, c.vid_stride_B)) return rc;
-  if (int rc = make_map(&mk, c.k, c.N, cols, c.vid_stride_B)) return rc;
-  if (int rc = make_map(&mv, c.v, c.N, cols, c.vid_stride_B)) return rc;
+  if (int rc = make_map(&mq, c.q, c.N, cols, c.vid_stride_B, kFp8)) return rc;
+  if (int rc = make_map(&mk, c.k, c.N, cols, c.vid_stride_B, kFp8)) return rc;
+  if (int rc = make_map(&mv, c.v, c.N, cols, c.vid_v_stride_B)) return rc;
   if (c.L > 0) {
-    if (int rc = make_map(&mqt, c.qt, c.L, cols, c.txt_stride_B)) return rc;
-    if (int rc = make_map(&mkt, c.kt, c.L, cols, c.txt_stride_B)) return rc;
+    if (int rc = make_map(&mqt, c.qt, c.L, cols, c.txt_stride_B, kFp8)) return rc;
+    if (int rc = make_map(&mkt, c.kt, c.L, cols, c.txt_stride_B, kFp8)) return rc;
     if (int rc = make_map(&mvt, c.vt, c.L, cols, c.vt_stride_B)) return rc;
   } else {
     mqt = mq; mkt = mk; mvt = mv;  // never read: there are no text tiles
@@ -977,7 +1004,7 @@ int launch(const AttnCall& c) {
   p.partial = c.partial;
   p.status = c.status;
   p.counter = c.status + 16;  // inside the status block, cleared before every launch
-  p.scale_log2 = c.scale * 1.4426950408889634f;
+  p.scale_log2 = c.scale * 1.4426950408889634f;  // e4m3: the dequantisation scales are folded into c.scale
   p.stall = take_stall() ? 1 : 0;
   p.vid_v8 = (reinterpret_cast<uintptr_t>(c.o_vid) % 32 == 0) && (c.o_stride_B % 32 == 0);
   p.txt_v8 = reinterpret_cast<uintptr_t>(c.partial) % 32 == 0;
@@ -988,11 +1015,14 @@ int launch(const AttnCall& c) {
   for (int i = 0; i < kRopePairs; ++i) p.theta[i] = c.rope_theta[i];
   size_t smem = kSmemBytes;
   if (kRope) {
-    smem = static_cast<size_t>(Cfg<HD>::kTab) + static_cast<size_t>(c.wt + c.wh + c.ww) * kRopeStride * 8 + 1024;
+    smem = static_cast<size_t>(Cfg<HD, kFp8>::kTab) + static_cast<size_t>(c.wt + c.wh + c.ww) * kRopeStride * 8 + 1024;
     if (smem > kRopeMaxSmem)
       return fail(WP_EUNSUPPORTED, "window %dx%dx%d too large for the RoPE table", c.wt, c.wh, c.ww);
   }
-  auto kern = attn_tc_kernel<HD, kRope>;
+  // Every variant asks for at least the bf16 footprint (kSmemBytes, more than
+  // half of an SM's shared memory) so that exactly one CTA, and one
+  // 512-column TMEM allocation, lives on an SM.
+  auto kern = attn_tc_kernel<HD, kRope, kFp8>;
   if (int rc = cuda_check(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(smem)),
                           "cudaFuncSetAttribute(attn_tc_kernel)"))
@@ -1015,8 +1045,12 @@ int launch(const AttnCall& c) {
 void stall_next_launches(int n) { g_stall_launches.store(n < 0 ? 0 : n); }
 
 int launch_attn_bf16_tc(const AttnCall& c) {
-  if (c.rope) return c.hd == 128 ? launch<128, true>(c) : fail(WP_EUNSUPPORTED, "RoPE attention needs head_dim 128");
-  return c.hd == 64 ? launch<64, false>(c) : launch<128, false>(c);
+  if (c.fp8) {
+    if (c.hd != 128 || c.rope) return fail(WP_EUNSUPPORTED, "e4m3 attention needs head_dim 128 and no RoPE");
+    return launch<128, false, true>(c);
+  }
+  if (c.rope) return c.hd == 128 ? launch<128, true, false>(c) : fail(WP_EUNSUPPORTED, "RoPE attention needs head_dim 128");
+  return c.hd == 64 ? launch<64, false, false>(c) : launch<128, false, false>(c);
 }
 
 }  // namespace wp

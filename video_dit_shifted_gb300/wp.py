@@ -51,6 +51,11 @@ SIGNATURES = {
     "wp_window_attn_static": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int,
                                        _vp, _vp, _vp, _c_i64, _vp, _vp, _vp, _c_i64,
                                        _vp, _c_i64, _vp, ctypes.c_float, _vp]),
+    "wp_window_attn_fp8": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                    _vp, _vp, _c_i64, _vp, _c_i64, _vp, _vp, _c_i64, _vp, _c_i64,
+                                    ctypes.c_float, ctypes.c_float, _vp, _c_i64, _vp, _vp, _c_sz,
+                                    ctypes.c_float, _vp]),
+    "wp_quantize_e4m3": (_c_int, [_vp, _c_i64, _c_int, _c_i64, _vp, _c_i64, ctypes.c_float, _vp]),
     "wp_read_status": (_c_int, [_vp, ctypes.POINTER(_c_int), _vp]),
     "wp_debug_stall_next": (_c_int, [_c_int]),
     "wp_last_error": (ctypes.c_char_p, []),
@@ -277,6 +282,37 @@ def window_attn(plan, layout, q, k, v, qt, kt, vt, o_vid, o_txt, workspace, scal
     return o_vid, o_txt
 
 
+def quantize_e4m3(src, dst, inv_scale, stream=None):
+    """dst = e4m3 codes of src * inv_scale (wp_quantize_e4m3 in include/wp.h).
+
+    src: 2-D bf16 CUDA tensor [rows, cols] (row stride may exceed cols);
+    dst: 2-D uint8 CUDA tensor of the same shape."""
+    rows, cols = src.shape
+    _check("wp_quantize_e4m3", lib().wp_quantize_e4m3(_ptr(src), rows, cols, src.stride(0) * 2, _ptr(dst),
+                                                      dst.stride(0), float(inv_scale), _stream_ptr(stream)))
+    return dst
+
+
+def window_attn_fp8(plan, layout, q8, k8, v, qt8, kt8, vt, q_scale, k_scale, o_vid, o_txt, workspace,
+                    scale=0.0, stream=None, out_layout=CANONICAL):
+    """Window attention with e4m3 q/k (wp_window_attn_fp8 in include/wp.h).
+
+    q8, k8: uint8 [N, heads, 128] views (e4m3 codes) sharing a row stride;
+    v: bf16 [N, heads, 128]; qt8, kt8: uint8 [L, heads, 128]; vt: bf16;
+    scores = (q8 * q_scale) . (k8 * k_scale) * scale."""
+    N, heads, hd = v.shape
+    L = vt.shape[0] if vt is not None else 0
+    if k8.stride(0) != q8.stride(0) or (L and kt8.stride(0) != qt8.stride(0)):
+        raise ValueError("q8 and k8 (and qt8 and kt8) must share one row stride")
+    _check("wp_window_attn_fp8", lib().wp_window_attn_fp8(
+        plan.handle, layout, out_layout, heads, hd, L, _ptr(q8), _ptr(k8), q8.stride(0), _ptr(v), v.stride(0) * 2,
+        _ptr(qt8 if L else None), _ptr(kt8 if L else None), qt8.stride(0) if L else 0,
+        _ptr(vt if L else None), vt.stride(0) * 2 if L else 0, float(q_scale), float(k_scale),
+        _ptr(o_vid), o_vid.stride(0) * 2, _ptr(o_txt if L else None), _ptr(workspace), workspace.numel(),
+        float(scale), _stream_ptr(stream)))
+    return o_vid, o_txt
+
+
 def debug_stall_next(launches):
     """Test hook: the next `launches` attention launches time out on purpose
     (wp_debug_stall_next in include/wp.h)."""
@@ -284,6 +320,8 @@ def debug_stall_next(launches):
 
 
 def read_status(workspace, stream=None):
+    """Device status word of an attention workspace; workspace=None reads the
+    fixed scratch of wp_window_attn_static on the current device."""
     st = _c_int()
     _check("wp_read_status", lib().wp_read_status(_ptr(workspace), ctypes.byref(st), _stream_ptr(stream)))
     return st.value
