@@ -340,6 +340,29 @@ def oracle_sample(wl_name, budget_s, seed_rows=None):
     return flops / t_used / 1e12, done, flops, t_used
 
 
+def oracle_relayout_sample(wl_name, reps=3):
+    """The oracle's re-layout (a numpy row gather by the inverted id table)
+    of the hidden rows [N, 2560] (bf16 bits as uint16) regular -> shifted on
+    the workload's grid, timed on the host: GB/s counting 2 * N * 5120 bytes
+    per re-layout, like the GPU's figure.  numpy's gather runs on one core."""
+    from oracle import permute as opm
+    from oracle import plan as op
+    w = WORKLOADS[wl_name]
+    g = (w["T"], w["H"], w["W"], w["nt"], w["nh"], w["nw"])
+    ids_r, ids_s = op.layout_tables(*g, op.REGULAR)[1], op.layout_tables(*g, op.SHIFTED)[1]
+    N = ids_r.size
+    rows = np.random.default_rng(0).integers(0, 1 << 16, size=(N, w["hidden"]), dtype=np.uint16)
+    opm.permute_rows(rows, ids_r, ids_s)                      # warm the pages
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        opm.permute_rows(rows, ids_r, ids_s)
+    secs = (time.perf_counter() - t0) / reps
+    nbytes = 2.0 * N * w["hidden"] * 2
+    return {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": "%d re-layouts of [%d, %d] bf16 rows regular -> shifted (%.2f GB each), %.3f s each"
+                      % (reps, N, w["hidden"], nbytes / 1e9, secs)}
+
+
 def host_threads():
     try:
         from threadpoolctl import threadpool_info
@@ -736,12 +759,13 @@ def run_ours(args):
                                                "L=256; 2 steps after 3 per variant (see bench.py "
                                                "full_schedule_measure)")
         extras["clocks"] = xclk.stop()
-    cpu = None
+    cpu = cpu_relayout = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tf, pairs, fl, secs = oracle_sample(args.workload, args.cpu_budget_s)
         cpu = {"value": tf, "unit": "TFLOP/s", "cores": host_threads(), "kind": "oracle",
                "sample": "%d (window, head) pairs of the regular layer (%.1f GFLOP, %.1f s), float64 numpy"
                          % (pairs, fl / 1e9, secs)}
+        cpu_relayout = oracle_relayout_sample(args.workload)
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -753,7 +777,7 @@ def run_ours(args):
                 "attn_tflops": attn_tflops, "relayout_gbs": relayout_gbs,
                 "roofline": roofline, "roofline_relayout": relayout, "roofline_rope": rope,
                 "rope_fused": rope_fused, "fp8_qk": fp8,
-                "cpu_baseline": cpu, "e2e": e2e,
+                "cpu_baseline": cpu, "cpu_baseline_relayout": cpu_relayout, "e2e": e2e,
                 "gpu_launches": wl.launches_per_step * args.steps, "clocks": clk}
         if extras is not None:
             line.update(extras_line(extras))
