@@ -97,6 +97,35 @@ def test_calls_validate_before_cuda(wp):
     plan.close()
 
 
+def test_e4m3_calls_validate_before_cuda(wp):
+    lib = wp.lib()
+    vp = ctypes.c_void_p
+    f = ctypes.c_float
+    # wp_quantize_e4m3(src, rows, cols, src_stride, dst, dst_stride, inv_scale, stream)
+    assert lib.wp_quantize_e4m3(None, 4, 32, 64, vp(4096), 32, f(1.0), None) == 1          # NULL src
+    assert lib.wp_quantize_e4m3(vp(4096), -1, 32, 64, vp(8192), 32, f(1.0), None) == 1     # negative rows
+    assert lib.wp_quantize_e4m3(vp(4096), 4, 24, 48, vp(8192), 32, f(1.0), None) == 2      # cols % 16
+    assert lib.wp_quantize_e4m3(vp(4104), 4, 32, 64, vp(8192), 32, f(1.0), None) == 2      # unaligned src
+    assert lib.wp_quantize_e4m3(vp(4096), 4, 32, 48, vp(8192), 32, f(1.0), None) == 2      # stride < row
+    for bad in (0.0, -2.0, float("inf"), float("nan")):
+        assert lib.wp_quantize_e4m3(vp(4096), 4, 32, 64, vp(8192), 32, f(bad), None) == 1
+    assert lib.wp_quantize_e4m3(vp(4096), 0, 32, 64, vp(8192), 32, f(1.0), None) == 0      # nothing to do
+    # wp_window_attn_fp8: head_dim, scales, strides, workspace, then the plan
+    plan = wp.Plan(2, 45, 80, 1, 3, 3)
+    size = ctypes.c_size_t()
+    assert lib.wp_attn_workspace_bytes(plan.handle, 1, 2, 128, 16, 0, ctypes.byref(size)) == 0
+    args = lambda hd, qs, qk_stride, v_stride, ws_bytes: (
+        plan.handle, 1, 0, 2, hd, 16, vp(256), vp(512), qk_stride, vp(1024), v_stride, vp(2048), vp(2304),
+        qk_stride, vp(4096), v_stride, f(qs), f(1.0), vp(8192), 512, vp(16384), vp(1 << 30), ws_bytes, f(0.0), None)
+    assert lib.wp_window_attn_fp8(*args(64, 1.0, 256, 512, size.value)) == 2      # head_dim 64
+    assert lib.wp_window_attn_fp8(*args(128, 0.0, 256, 512, size.value)) == 1     # scale
+    assert lib.wp_window_attn_fp8(*args(128, 1.0, 240, 512, size.value)) == 2     # q/k stride < row (256 B)
+    assert lib.wp_window_attn_fp8(*args(128, 1.0, 256, 256, size.value)) == 2     # v stride < row (512 B)
+    assert lib.wp_window_attn_fp8(*args(128, 1.0, 256, 512, 64)) == 1             # workspace too small
+    assert lib.wp_window_attn_fp8(*args(128, 1.0, 256, 512, size.value)) in (3, 6)  # not uploaded
+    plan.close()
+
+
 def test_debug_stall_hook_validates(wp):
     lib = wp.lib()
     assert lib.wp_debug_stall_next(-1) == 1

@@ -287,6 +287,8 @@ def quantize_e4m3(src, dst, inv_scale, stream=None):
 
     src: 2-D bf16 CUDA tensor [rows, cols] (row stride may exceed cols);
     dst: 2-D uint8 CUDA tensor of the same shape."""
+    if src.dtype != torch.bfloat16 or dst.dtype != torch.uint8 or src.dim() != 2 or dst.shape != src.shape:
+        raise TypeError("quantize_e4m3 takes a 2-D bfloat16 src and a uint8 dst of the same shape")
     rows, cols = src.shape
     _check("wp_quantize_e4m3", lib().wp_quantize_e4m3(_ptr(src), rows, cols, src.stride(0) * 2, _ptr(dst),
                                                       dst.stride(0), float(inv_scale), _stream_ptr(stream)))
@@ -302,6 +304,8 @@ def window_attn_fp8(plan, layout, q8, k8, v, qt8, kt8, vt, q_scale, k_scale, o_v
     scores = (q8 * q_scale) . (k8 * k_scale) * scale."""
     N, heads, hd = v.shape
     L = vt.shape[0] if vt is not None else 0
+    if q8.dtype != torch.uint8 or k8.dtype != torch.uint8 or v.dtype != torch.bfloat16:
+        raise TypeError("window_attn_fp8 takes uint8 (e4m3 code) q8/k8 and bfloat16 v")
     if k8.stride(0) != q8.stride(0) or (L and kt8.stride(0) != qt8.stride(0)):
         raise ValueError("q8 and k8 (and qt8 and kt8) must share one row stride")
     _check("wp_window_attn_fp8", lib().wp_window_attn_fp8(
