@@ -170,6 +170,38 @@ def test_1080p_sampled(vds):
     _sampled_check(vds, (21, 68, 120, 4, 3, 3), 24, 128, 256, text_heads=(5, 17))
 
 
+def test_full_schedule_grid_sampled(vds):
+    """The 32-layer schedule's grid (T=30, 90x160: 432,000 tokens, windows of
+    8x15x27, 144 regular and 245 shifted) at full size."""
+    _sampled_check(vds, (30, 90, 160, 4, 3, 3), 24, 128, 256, text_heads=(11,))
+
+
+@pytest.mark.parametrize("L", [0, 5])
+def test_single_token_grid(vds, L):
+    """T = H = W = 1: one window holding one token.  Without text its only
+    key is itself, so the output is its own v row exactly (p = 1); with text
+    it is the oracle's attention over [1 video ; L text] keys."""
+    from video_dit_shifted_gb300 import synth
+    grid, heads, hd = (1, 1, 1, 1, 1, 1), 3, 128
+    plan = vds.Plan(*grid, device="cuda")
+    for layout in (op.REGULAR, op.SHIFTED):
+        x = synth.attention_inputs(1, max(L, 1), heads, hd, torch.bfloat16, "cuda", base_seed=29)
+        qt, kt, vt = (x["qt"], x["kt"], x["vt"]) if L else (None, None, None)
+        o = torch.full((1, heads, hd), float("nan"), dtype=torch.bfloat16, device="cuda")
+        t = torch.full((max(L, 1), heads, hd), float("nan"), dtype=torch.bfloat16, device="cuda")
+        ws = vds.make_workspace(plan, layout, heads, hd, L, vds.BF16, "cuda")
+        vds.window_attn(plan, layout, x["q"], x["k"], x["v"], qt, kt, vt, o, t[:L] if L else None, ws)
+        assert vds.read_status(ws) == 0
+        if L == 0:
+            assert torch.equal(o, x["v"])
+        else:
+            off, ids = op.layout_tables(*grid, layout)
+            ref_o, ref_t = oa.window_attention(*(_np(x[n]) for n in ("q", "k", "v", "qt", "kt", "vt")), off, ids)
+            assert np.abs(_np(o) - ref_o).max() <= TOL[torch.bfloat16]
+            assert np.abs(_np(t) - oa.text_mean(ref_t)).max() <= TOL[torch.bfloat16]
+    plan.close()
+
+
 def test_bad_alignment_rejected(vds):
     plan = vds.Plan(2, 45, 80, 1, 3, 3, device="cuda")
     from video_dit_shifted_gb300 import synth
