@@ -206,6 +206,9 @@ int wp_attn_workspace_bytes(const wp_plan* plan, int layout, int heads,
  *   workspace at least wp_attn_workspace_bytes; its status word is cleared
  *             at the start of the call.
  * All rows of q/k/v (including rows of neighbouring windows) must be finite.
+ * An output row the plan's device tables place outside [0, N) (possible only
+ * if the plan's buffer changed after wp_plan_upload) is not written, and
+ * WP_EDEVICE goes to the status word.
  * Supported (WP_EUNSUPPORTED otherwise): head_dim 64 or 128; pointers and
  * strides multiples of 16 bytes; heads*head_dim*elem <= stride.
  * WP_EINVAL: null pointer, heads < 1, L < 0, layout not REGULAR/SHIFTED,

@@ -548,3 +548,52 @@ def test_text_sum_over_many_windows(vds):
         torch.cuda.synchronize()
         assert torch.equal(o1, o3) and torch.equal(t1, t3), layout
     plan.close()
+
+
+@pytest.mark.parametrize("dtype,hd", [(torch.bfloat16, 128), (torch.float32, 64)])
+def test_out_of_range_table_entry_is_reported_not_written(vds, dtype, hd):
+    """The plan's device tables live in a caller-owned buffer that must not
+    change after the upload.  If an output-row entry is changed to lie past
+    the last row anyway, the kernel records WP_EDEVICE in the status word and
+    writes nothing for that row; every other row is still right.  The entry
+    used here is N + 3 and the output sits inside a larger buffer with guard
+    rows, so even an unchecked store would land in memory this test owns."""
+    from video_dit_shifted_gb300 import synth
+    grid, heads, L = (3, 30, 40, 2, 3, 3), 2, 20
+    plan = vds.Plan(*grid, device="cuda")
+    N = plan.N
+    code = vds.BF16 if dtype == torch.bfloat16 else vds.FP32
+    off, ids = op.layout_tables(*grid, op.REGULAR)
+    # find the regular layout's id table in the device buffer
+    nbytes = plan.device_bytes()
+    start = (-plan.dev_buf.data_ptr()) % 256
+    tab = plan.dev_buf[start:start + nbytes].view(torch.int32)
+    host = tab.cpu().numpy()
+    cand = [i for i in np.flatnonzero(host == ids[0]) if i + N <= host.size and np.array_equal(host[i:i + N], ids)]
+    # the layout's own table comes first; the fused canonical -> regular
+    # permutation table further on holds the same values
+    assert len(cand) >= 1
+    k = int(off[1]) + 5                                   # a token of window 1
+    x = synth.attention_inputs(N, L, heads, hd, dtype, "cuda", base_seed=31)
+    big = torch.full((N + 8, heads, hd), 7.0, dtype=dtype, device="cuda")
+    o = big[:N]
+    t = torch.empty((L, heads, hd), dtype=dtype, device="cuda")
+    ws = vds.make_workspace(plan, op.REGULAR, heads, hd, L, code, "cuda")
+    tab[cand[0] + k] = N + 3
+    try:
+        o.fill_(float("nan"))
+        vds.window_attn(plan, op.REGULAR, x["q"], x["k"], x["v"], x["qt"], x["kt"], x["vt"], o, t, ws)
+        assert vds.read_status(ws) == 5                   # WP_EDEVICE
+        assert torch.all(big[N:] == 7.0)                  # nothing written past the output
+        ref_o, _ = oa.window_attention(*(_np(x[n]) for n in ("q", "k", "v", "qt", "kt", "vt")), off, ids)
+        got = _np(o)
+        missing = int(ids[k])                             # the row that entry should have written
+        assert np.all(np.isnan(got[missing]))
+        keep = np.ones(N, bool)
+        keep[missing] = False
+        assert np.abs(got[keep] - ref_o[keep]).max() <= TOL[dtype]
+    finally:
+        tab[cand[0] + k] = int(ids[k])
+    vds.window_attn(plan, op.REGULAR, x["q"], x["k"], x["v"], x["qt"], x["kt"], x["vt"], o, t, ws)
+    assert vds.read_status(ws) == 0
+    plan.close()

@@ -39,6 +39,8 @@ struct F32Params {
   float* o_vid;
   float* partial;
   const int32_t *win_off, *ids;
+  int64_t n_rows;  // rows of o_vid (N)
+  int* status;
   int heads, L, qblocks;
   float scale;
 };
@@ -114,7 +116,11 @@ __global__ void __launch_bounds__(kF32Rows * kF32Tpr) attn_f32_kernel(F32Params 
   }
   if (!live) return;
   const float inv = 1.f / l;
-  const int64_t orow = p.ids ? static_cast<int64_t>(p.ids[a + r]) : static_cast<int64_t>(a + r);
+  const int64_t orow = r < n_w ? (p.ids ? static_cast<int64_t>(p.ids[a + r]) : static_cast<int64_t>(a + r)) : 0;
+  if (r < n_w && static_cast<uint64_t>(orow) >= static_cast<uint64_t>(p.n_rows)) {
+    atomicCAS(p.status, 0, WP_EDEVICE);  // table entry outside the output (plan buffer changed): not written
+    return;
+  }
   float* out = r < n_w ? p.o_vid + orow * p.o_stride + h * HD
                        : p.partial + ((static_cast<int64_t>(w) * p.L + (r - n_w)) * p.heads + h) * HD;
 #pragma unroll
@@ -170,6 +176,8 @@ int launch_attn_f32(const AttnCall& c) {
   p.partial = c.partial;
   p.win_off = c.win_off;
   p.ids = c.ids;
+  p.n_rows = c.N;
+  p.status = c.status;
   p.heads = c.heads;
   p.L = c.L;
   p.qblocks = (c.max_tokens + c.L + kF32Rows - 1) / kF32Rows;

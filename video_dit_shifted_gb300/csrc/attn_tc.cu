@@ -131,6 +131,7 @@ struct TcParams {
   int nwin, L, heads, text_tiles, total_pairs;
   __nv_bfloat16* o_vid;
   int64_t o_stride;  // elements
+  int64_t n_rows;    // rows of o_vid (N): every table entry must lie below it
   float* partial;
   int* status;
   int* counter;  // next work item (zero at launch)
@@ -873,8 +874,13 @@ __global__ void __launch_bounds__(kRope ? kRopeThreads : kThreads, 1)
       const float inv_l = 1.f / l_run;
       if (t < x.vt) {
         const int tok = t * kBM + r;
-        if (tok < x.n_w) {
-          const int64_t orow = p.ids ? static_cast<int64_t>(__ldg(p.ids + x.a + tok)) : static_cast<int64_t>(x.a + tok);
+        const int64_t orow =
+            tok < x.n_w ? (p.ids ? static_cast<int64_t>(__ldg(p.ids + x.a + tok)) : static_cast<int64_t>(x.a + tok)) : 0;
+        // An output row outside [0, N) can only come from a plan buffer
+        // changed after its upload: record it and write nothing there.
+        if (tok < x.n_w && static_cast<uint64_t>(orow) >= static_cast<uint64_t>(p.n_rows))
+          atomicCAS(p.status, 0, WP_EDEVICE);
+        else if (tok < x.n_w) {
           __nv_bfloat16* dst = p.o_vid + orow * p.o_stride + x.h * HD;
           if (p.vid_v8) {
             // 32-byte stores: whole sectors, half the instructions.
@@ -1001,6 +1007,7 @@ int launch(const AttnCall& c) {
   p.total_pairs = c.total_pairs;
   p.o_vid = static_cast<__nv_bfloat16*>(c.o_vid);
   p.o_stride = c.o_stride_B / 2;
+  p.n_rows = c.N;
   p.partial = c.partial;
   p.status = c.status;
   p.counter = c.status + 16;  // inside the status block, cleared before every launch
