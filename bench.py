@@ -740,15 +740,25 @@ def run_ours(args):
     extras = None
     if world == 1 and not args.no_extras:
         torch.cuda.empty_cache()
-        xclk = ClockSampler(dev.index)
-        xclk.start()
-        sw = sweep_measure(dev, steps=5, warmup=3)
+
+        def clocked(fn):
+            c = ClockSampler(dev.index)
+            c.start()
+            out = fn()
+            return out, c.stop()
+
+        a720, clk720 = clocked(lambda: layer_measure("720p", dev, reps=20, warmup=3))
+        sw, clksw = clocked(lambda: sweep_measure(dev, steps=5, warmup=3))
+        fs, clkfs = clocked(lambda: full_schedule_measure(dev, steps=2, warmup=3))
+        a720["clocks"] = clk720
+        fs["clocks"] = clkfs
         extras = {
-            "attn_720p": layer_measure("720p", dev, reps=20, warmup=3),
+            "attn_720p": a720,
             "relayout_sweep": {k: sw[k] for k in ("median_gbs", "frac", "min_gbs", "max_gbs", "points_in_median",
                                                   "peak", "l2")},
-            "full_schedule": full_schedule_measure(dev, steps=2, warmup=3),
+            "full_schedule": fs,
         }
+        extras["relayout_sweep"]["clocks"] = clksw
         extras["relayout_sweep"]["workload"] = ("[N,2560] bf16 rows, regular->shifted and back, grids 45x80/68x120/"
                                                 "90x160 x T in {5,21,30}; median of 5 launches per point, L2 flushed "
                                                 "before each; median over the points above 4x L2")
@@ -758,7 +768,6 @@ def run_ours(args):
         extras["full_schedule"]["workload"] = ("32 alternating layers on T=30 H=90 W=160 (N=432000), 24x128 heads, "
                                                "L=256; 2 steps after 3 per variant (see bench.py "
                                                "full_schedule_measure)")
-        extras["clocks"] = xclk.stop()
     cpu = cpu_relayout = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tf, pairs, fl, secs = oracle_sample(args.workload, args.cpu_budget_s)
@@ -844,8 +853,7 @@ def extras_line(x):
     return {"attn_720p": x["attn_720p"], "relayout_sweep": x["relayout_sweep"],
             "full_schedule": {"workload": fs["workload"], "attn_tflop_per_step": fs["attn_tflop_per_step"],
                               "qkv": fs["qkv"], "unfused": fs["unfused"], "fused": fs["fused"],
-                              "fused_saves": fs["fused_saves"]},
-            "extras_clocks": x["clocks"]}
+                              "fused_saves": fs["fused_saves"], "clocks": fs["clocks"]}}
 
 
 def main():
