@@ -597,3 +597,27 @@ def test_out_of_range_table_entry_is_reported_not_written(vds, dtype, hd):
     vds.window_attn(plan, op.REGULAR, x["q"], x["k"], x["v"], x["qt"], x["kt"], x["vt"], o, t, ws)
     assert vds.read_status(ws) == 0
     plan.close()
+
+
+@pytest.mark.parametrize("grid,heads,hd,L", [((21, 68, 120, 4, 3, 3), 24, 128, 256),
+                                             ((2, 30, 40, 1, 2, 2), 40, 128, 1000),
+                                             ((3, 30, 40, 2, 3, 3), 2, 64, 300)])
+def test_text_mean_is_the_ordered_fp32_mean(vds, grid, heads, hd, L):
+    """o_txt must be, bit for bit, the window-ordered fp32 sum of the
+    per-window text outputs T_w that the attention kernel leaves in the
+    workspace, divided by the window count and rounded to bf16 (computed
+    here on the host, one window after the other)."""
+    from video_dit_shifted_gb300 import synth
+    plan = vds.Plan(*grid, device="cuda")
+    x = synth.attention_inputs(plan.N, L, heads, hd, torch.bfloat16, "cuda", base_seed=37)
+    for layout in (op.REGULAR, op.SHIFTED):
+        o_vid, o_txt, ws = _run(vds, plan, layout, x, heads, hd, L, torch.bfloat16)
+        nwin = plan.info(layout)["nwin"]
+        start = 256                                     # after the status block
+        part = ws[start:start + nwin * L * heads * hd * 4].view(torch.float32).view(nwin, L, heads, hd).cpu().numpy()
+        acc = np.zeros(part.shape[1:], dtype=np.float32)
+        for w in range(nwin):
+            acc = acc + part[w]
+        want = torch.from_numpy(acc / np.float32(nwin)).to(torch.bfloat16)
+        assert torch.equal(o_txt.cpu(), want), layout
+    plan.close()
