@@ -9,9 +9,10 @@
   rounding's (3 mantissa bits: each q, k element carries up to 2^-4
   relative error); it is measured here and bounded by FP8_TOL, a figure
   taken from these measurements, not from the pages.  Measured on a GB300:
-  0.029 (3x30x40 grid, windows of 1200-2430 tokens, L = 300), 0.044 (the
-  PR1 grid, L = 16), 0.118 (segments of 53 keys, where a softmax averages
-  fewer scores and their rounding shows more).
+  0.029 (3x30x40 grid, windows of 1200-2430 tokens, L = 300), 0.081 (the
+  same grid without text), 0.044 (the PR1 grid, L = 16), 0.118 (segments
+  of 53 keys, where a softmax averages fewer scores and their rounding
+  shows more).
 """
 import numpy as np
 import pytest
@@ -90,7 +91,7 @@ def _packed_codes(x, names=("q", "k")):
 
 
 @pytest.mark.parametrize("grid,heads,L", [((3, 30, 40, 2, 3, 3), 2, 300), ((2, 45, 80, 1, 3, 3), 3, 16),
-                                          ((2, 45, 80, 1, 9, 16), 2, 3)])
+                                          ((2, 45, 80, 1, 9, 16), 2, 3), ((3, 30, 40, 2, 3, 3), 2, 0)])
 def test_fp8_attention_matches_oracle(vds, grid, heads, L):
     from video_dit_shifted_gb300 import synth
     plan = vds.Plan(*grid, device="cuda")
@@ -109,8 +110,11 @@ def test_fp8_attention_matches_oracle(vds, grid, heads, L):
             if out != op.CANONICAL:        # output row r holds canonical token ids[r]
                 got = got[np.argsort(ids)]
             assert np.abs(got - ref_o).max() <= TOL, (layout, out)
-            assert np.abs(_np(t) - oa.text_mean(ref_t)).max() <= TOL, (layout, out)
-            errs.append(max(np.abs(got - exact_o).max(), np.abs(_np(t) - oa.text_mean(exact_t)).max()))
+            err = np.abs(got - exact_o).max()
+            if L:
+                assert np.abs(_np(t) - oa.text_mean(ref_t)).max() <= TOL, (layout, out)
+                err = max(err, np.abs(_np(t) - oa.text_mean(exact_t)).max())
+            errs.append(err)
     print("e4m3 attention, max abs error against the unquantised oracle:", max(errs))
     assert max(errs) <= FP8_TOL
     plan.close()
