@@ -711,6 +711,7 @@ def run_ours(args):
     peaks_r, _ = load_peaks()
     rope = {"bound": "hbm", "achieved": rope_bytes / (rope_ms * 1e-3) / 1e9, "peak": peaks_r["hbm_gbs"],
             "unit": "GB/s", "frac": rope_bytes / (rope_ms * 1e-3) / 1e9 / peaks_r["hbm_gbs"], "ms": rope_ms,
+            "traffic": recorded_traffic("rope.cu", "rope_1080p") if args.workload == "1080p" else None,
             "bytes_per_launch": rope_bytes, "kernel": "rope_kernel (regular layout, q and k in place)"}
     # The same regular layer with the RoPE applied inside the attention kernel
     # (wp_window_attn_rope, un-rotated q/k in) against the RoPE pass followed
