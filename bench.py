@@ -731,7 +731,8 @@ def run_ours(args):
     if vds.read_status(ws_rope) != 0:
         raise RuntimeError("device status set by wp_window_attn_rope")
     attn_reg_ms = sum(attn_reg) / args.steps
-    rope_fused = {"kernel": "attn_tc_kernel with RoPE warps (wp_window_attn_rope), regular layer",
+    rope_fused = {"kernel": "wp_window_attn_rope, regular layer: k rotated once into the workspace "
+                            "(rope_k_copy_kernel), Q tiles rotated inside attn_tc_kernel",
                   "ms_fused": fused_ms, "tflops_fused": f_reg / (fused_ms * 1e-3) / 1e12,
                   "ms_rope_then_attn": rope_ms + attn_reg_ms, "ms_attn": attn_reg_ms, "ms_rope": rope_ms}
     del ws_rope

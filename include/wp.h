@@ -239,22 +239,24 @@ int wp_window_attn_to(const wp_plan* plan, int layout, int out_layout, int heads
 
 /* wp_attn_rope_workspace_bytes -- device workspace wp_window_attn_rope
  * needs: wp_attn_workspace_bytes plus the rotated text q and k
- * (2 * L * heads * head_dim bf16 values). */
+ * (2 * L * heads * head_dim bf16 values), then, from the next multiple of
+ * 1024 bytes, the rotated video k (N * heads * head_dim bf16 values). */
 int wp_attn_rope_workspace_bytes(const wp_plan* plan, int layout, int heads,
                                  int head_dim, int L, int dtype, size_t* bytes);
 
 /* wp_window_attn_rope -- wp_window_attn_to on UN-rotated q and k: applies
  * the window-local 3D RoPE of wp_rope ("Window-Aligned Sequence Parallelism
  * (SeedVR2)", §Reference quirks reproduced on purpose; same positions,
- * angles base^(-2i/42) and channel pairs) inside the attention kernel, so
- * no separate pass reads and writes q and k.  q, k, qt, kt are the
- * projections before RoPE and are not modified; v, vt, the outputs, the
- * scatter (`out_layout`) and the text mean are as in wp_window_attn_to.
- * The text q/k are rotated once per call into the workspace (shared by every
- * window); video Q and K tiles are rotated in shared memory after they land,
- * in bf16 arithmetic (cos, sin rounded to bf16; two roundings per value),
- * so results agree with wp_rope followed by wp_window_attn_to to within
- * the bf16 attention tolerance, not bit for bit.
+ * angles base^(-2i/42) and channel pairs) as part of the call, so that q
+ * is never rotated in HBM.  q, k, qt, kt are the projections before RoPE
+ * and are not modified; v, vt, the outputs, the scatter (`out_layout`) and
+ * the text mean are as in wp_window_attn_to.  k and the text q/k, read by
+ * many work items, are rotated once per call into the workspace (in fp32,
+ * one rounding to bf16: the values wp_rope writes); each video Q tile,
+ * read by one work item, is rotated in shared memory after it lands, in
+ * bf16 arithmetic (cos, sin rounded to bf16; two roundings per value), so
+ * results agree with wp_rope followed by wp_window_attn_to to within the
+ * bf16 attention tolerance, not bit for bit.
  * Supported (WP_EUNSUPPORTED otherwise): dtype WP_BF16, head_dim 128, the
  * plan's window size (wt + wh + ww) <= 196 (the cos/sin table lives in
  * shared memory), the alignment rules of wp_window_attn.  WP_EINVAL:

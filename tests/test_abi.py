@@ -82,10 +82,12 @@ def test_calls_validate_before_cuda(wp):
     fsize = ctypes.c_size_t()
     assert lib.wp_attn_workspace_bytes(plan.handle, 1, 2, 128, 16, 1, ctypes.byref(fsize)) == 0
     assert fsize.value == size.value
-    # RoPE attention: the workspace adds the rotated text q and k (bf16)
+    # RoPE attention: the workspace adds the rotated text q and k (bf16), then
+    # (1024-byte aligned) the rotated video k [N, heads, 128] bf16, N = 2*45*80
     rsize = ctypes.c_size_t()
     assert lib.wp_attn_rope_workspace_bytes(plan.handle, 1, 2, 128, 16, 0, ctypes.byref(rsize)) == 0
-    assert rsize.value == size.value + 2 * 16 * 2 * 128 * 2
+    krot = (size.value + 2 * 16 * 2 * 128 * 2 + 1023) // 1024 * 1024
+    assert rsize.value == krot + 7200 * 2 * 128 * 2
     rargs = lambda layout, hd, dtype, ws_bytes, base: (
         plan.handle, layout, 0, 2, hd, 16, dtype, vp(256), vp(512), vp(768), 8192, vp(1024), vp(1280), vp(1536),
         8192, vp(4096), 8192, vp(2048), vp(1 << 30), ws_bytes, ctypes.c_float(0.0), ctypes.c_float(base), None)

@@ -199,14 +199,24 @@ using namespace wp;
 namespace {
 
 // Partial text outputs T_w start at kStatusBytes; with rope, the rotated
-// text q and k (bf16, packed rows) follow them.
+// text q and k (bf16, packed rows) follow them, then, 1024-byte aligned,
+// the rotated video k (bf16, packed rows [N, heads * hd]).
 int64_t partial_bytes(const wp_plan* plan, int layout, int heads, int hd, int L) {
   return static_cast<int64_t>(plan->lay[layout].nwin) * L * heads * hd * 4;
 }
 
+int64_t text_rot_offset(const wp_plan* plan, int layout, int heads, int hd, int L) {
+  return static_cast<int64_t>(kStatusBytes) + partial_bytes(plan, layout, heads, hd, L);
+}
+
+int64_t krot_offset(const wp_plan* plan, int layout, int heads, int hd, int L) {
+  const int64_t end = text_rot_offset(plan, layout, heads, hd, L) + 2 * static_cast<int64_t>(L) * heads * hd * 2;
+  return (end + 1023) / 1024 * 1024;
+}
+
 int workspace_bytes(const wp_plan* plan, int layout, int heads, int hd, int L, size_t* bytes, bool rope = false) {
-  const int64_t text_rot = rope ? 2 * static_cast<int64_t>(L) * heads * hd * 2 : 0;
-  *bytes = kStatusBytes + static_cast<size_t>(partial_bytes(plan, layout, heads, hd, L) + text_rot);
+  *bytes = rope ? static_cast<size_t>(krot_offset(plan, layout, heads, hd, L) + plan->N * heads * hd * 2)
+                : kStatusBytes + static_cast<size_t>(partial_bytes(plan, layout, heads, hd, L));
   return WP_OK;
 }
 
@@ -322,10 +332,19 @@ int window_attn_impl(const wp_plan* plan, int layout, int out_layout, int heads,
 
   if (int rc = cuda_check(cudaMemsetAsync(workspace, 0, kStatusBytes, c.stream), "cudaMemsetAsync(status)"))
     return rc;
+  if (rope) {
+    // Every video K tile is read by every work item of its (window, head):
+    // rotate k once, into the workspace, and let the kernel read the copy
+    // (the kernel rotates only the video Q tiles, each read by one item).
+    char* krot = static_cast<char*>(workspace) + krot_offset(plan, layout, heads, head_dim, L);
+    if (int rc = rope_k_copy(plan, layout, k, vid_row_stride_B, krot, heads, L, rope_base, c.stream)) return rc;
+    c.k = krot;
+    c.vid_k_stride_B = static_cast<int64_t>(heads) * head_dim * 2;
+  }
   if (rope && L > 0) {
     // The text rows are shared by every window: rotate them once, into the
     // workspace, and let the kernel read the copies.
-    char* rot = static_cast<char*>(workspace) + kStatusBytes + partial_bytes(plan, layout, heads, head_dim, L);
+    char* rot = static_cast<char*>(workspace) + text_rot_offset(plan, layout, heads, head_dim, L);
     void* qt_rot = rot;
     void* kt_rot = rot + static_cast<int64_t>(L) * heads * head_dim * 2;
     if (int rc = rope_text_copy(qt, kt, txt_row_stride_B, qt_rot, kt_rot, L, heads, rope_base, c.stream)) return rc;

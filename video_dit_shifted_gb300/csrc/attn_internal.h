@@ -21,6 +21,7 @@ struct AttnCall {
   int layout, heads, hd, L, dtype;
   const void *q, *k, *v;
   int64_t vid_stride_B;    // q and k
+  int64_t vid_k_stride_B = 0;  // k, when it differs from q (0: vid_stride_B)
   int64_t vid_v_stride_B;  // v
   const void *qt, *kt, *vt;
   int64_t txt_stride_B;  // qt and kt
@@ -43,8 +44,8 @@ struct AttnCall {
   // q, k, qt, kt are e4m3 codes (wp_window_attn_fp8); their dequantisation
   // scales are folded into `scale`.
   bool fp8 = false;
-  // Window-local RoPE applied inside the kernel (wp_window_attn_rope): the
-  // text q/k passed in are already rotated.
+  // Window-local RoPE of the video Q tiles applied inside the kernel
+  // (wp_window_attn_rope): k and the text q/k passed in are already rotated.
   bool rope = false;
   const int32_t* boxes = nullptr;  // device: t0,t1,h0,h1,w0,w1 per window
   int wt = 0, wh = 0, ww = 0;      // window size
@@ -70,5 +71,10 @@ void rope_theta(float rope_base, float* theta21);
 // place with the text positions (l, l, l) of wp_rope.
 int rope_text_copy(const void* qt, const void* kt, int64_t txt_stride_B, void* qt_out, void* kt_out, int L,
                    int heads, float rope_base, cudaStream_t stream);
+// Writes the N video rows of k (bf16, heads x 128 per row, layout order of
+// `layout`, row stride vid_stride_B) rotated with wp_rope's window-local
+// positions (text length L) to k_out (packed rows); k is not changed.
+int rope_k_copy(const wp_plan* plan, int layout, const void* k, int64_t vid_stride_B, void* k_out, int heads, int L,
+                float rope_base, cudaStream_t stream);
 
 }  // namespace wp

@@ -36,8 +36,11 @@
 //   warp 9      TMEM allocator (512 columns: S0, S1, O0, O1) and MMA issuer:
 //               S_i = Q_i K_j^T (both operands in shared memory) and
 //               O_i += P_i V_j (P from TMEM, V MN-major);
-//   warps 10-11 (RoPE kernels only) the window-local RoPE of video Q and K
-//               tiles in shared memory between the TMA and the MMA.
+//   warps 10-11 (RoPE kernels only) the window-local RoPE of the video Q
+//               tiles in shared memory between the TMA and the MMA; the
+//               RoPE kernels read K already rotated (a separate pass writes
+//               every video K row once, rotated, to the workspace), so K/V
+//               payloads go from the TMA to the MMA as in the plain kernels.
 // The two query tiles share every K/V tile, and the issue order
 // S0(j) S1(j) PV0(j) S0(j+1) PV1(j) S1(j+1) ... lets one tile's softmax run
 // while the tensor core works on the other.  The issuer is the whole warp 9,
@@ -76,7 +79,7 @@ namespace {
 constexpr int kBM = 128;  // query rows per tile (TMEM lanes)
 constexpr int kBN = 128;  // keys per K/V tile
 constexpr int kThreads = 320;       // warps 0-7 softmax, 8 TMA, 9 MMA
-constexpr int kRopeThreads = 384;   // RoPE kernels: + warps 10-11 rotating Q and K tiles
+constexpr int kRopeThreads = 384;   // RoPE kernels: + warps 10-11 rotating Q tiles
 constexpr int kRopeWarp0 = 10;
 constexpr int kRopePairs = 21;      // rotated pairs per axis at head_dim 128 (42 channels)
 constexpr int kRopeStride = 22;     // table entries per axis position (21 + 1 pad: 16-byte pairs)
@@ -113,7 +116,7 @@ struct Barriers {
   uint64_t q_full, q_empty;
   uint64_t pl_full[2], pl_empty[2];  // K/V payload slots (see the producer)
   uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
-  uint64_t q_ready, pl_ready[2];     // RoPE kernels: Q / payload rotated
+  uint64_t q_ready;                  // RoPE kernels: Q rotated
   uint64_t item_full[4], item_empty[4];  // ring of work-item indices (see the producer)
   uint64_t mma_done;
   uint64_t stall;                    // test hook: a barrier nothing arrives at
@@ -516,7 +519,6 @@ __global__ void __launch_bounds__(kRope ? kRopeThreads : kThreads, 1)
     }
     if (kRope) {
       mbar_init(bar(bars->q_ready), 64);
-      for (int s = 0; s < 2; ++s) mbar_init(bar(bars->pl_ready[s]), 64);
     }
     // A CTA of this launch already failed: skip the work so that a broken
     // launch ends quickly instead of timing out CTA after CTA.
@@ -656,7 +658,7 @@ __global__ void __launch_bounds__(kRope ? kRopeThreads : kThreads, 1)
       // One query tile's share of step j: O_i += P_i V_j, then S_i = Q_i K_{j+1}^T.
       // The tile index is a compile-time constant so that every phase counter
       // and TMEM address stays in registers.
-      auto tile_step = [&](auto I, int j, int s, int sn, bool more, int cs, int co, uint32_t ready_parity) -> bool {
+      auto tile_step = [&](auto I, int j, int s, int sn, bool more, int cs, int co) -> bool {
         constexpr int i = decltype(I)::value;
         if (!wait_phase(bar(bars->p_full[i]), (cs + j) & 1, abort_flag, p.status)) return false;
         // O_i is overwritten by this item's first P V: the previous item's
@@ -666,10 +668,6 @@ __global__ void __launch_bounds__(kRope ? kRopeThreads : kThreads, 1)
         tc_fence_after();
         issue_pv(i, s, j == 0);
         if (more) {
-          if (kRope && i == 0) {
-            if (!wait_phase(bar(bars->pl_ready[sn]), ready_parity, abort_flag, p.status)) return false;
-            tc_fence_after();
-          }
           issue_qk(i, sn);
           mma_commit(bar(bars->s_full[i]));
         } else {
@@ -688,10 +686,9 @@ __global__ void __launch_bounds__(kRope ? kRopeThreads : kThreads, 1)
           break;
         const Item x = decode_item(p, it);
         // payload [K_0]
-        // (RoPE kernels: the rotated Q and payload, released by warps 10-11.)
+        // (RoPE kernels: Q once warps 10-11 have rotated it.)
         if (!(good = wait_phase(kRope ? bar(bars->q_ready) : bq_full, k & 1, abort_flag, p.status) &&
-                     wait_phase(kRope ? bar(bars->pl_ready[e & 1]) : bar(bars->pl_full[e & 1]), (e >> 1) & 1,
-                                abort_flag, p.status)))
+                     wait_phase(bar(bars->pl_full[e & 1]), (e >> 1) & 1, abort_flag, p.status)))
           break;
         tc_fence_after();
         issue_qk(0, e & 1);
@@ -706,17 +703,9 @@ __global__ void __launch_bounds__(kRope ? kRopeThreads : kThreads, 1)
         for (int j = 0; j < x.nkv; ++j, ++e) {
           const int s = e & 1;  // payload [V_j, K_{j+1}]
           const bool more = j + 1 < x.nkv;
-          // RoPE kernels: P V needs only V_j (landed), Q K^T the rotated K_{j+1}
-          // (pl_ready, waited inside tile_step), so the rotation overlaps P V.
           if (!(good = wait_phase(bar(bars->pl_full[s]), (e >> 1) & 1, abort_flag, p.status))) break;
-          if (!(good = tile_step(std::integral_constant<int, 0>{}, j, s, s, more, cs0, co0, (e >> 1) & 1))) break;
-          if (x.nq > 1 && !(good = tile_step(std::integral_constant<int, 1>{}, j, s, s, more, cs1, co1, (e >> 1) & 1)))
-            break;
-          // RoPE kernels: the item's last payload (V only) is released only after
-          // the RoPE warps have passed it too, so that they can never fall a
-          // payload behind the producer (a parity wait would then alias).
-          if (kRope && !more &&
-              !(good = wait_phase(bar(bars->pl_ready[s]), (e >> 1) & 1, abort_flag, p.status)))
+          if (!(good = tile_step(std::integral_constant<int, 0>{}, j, s, s, more, cs0, co0))) break;
+          if (x.nq > 1 && !(good = tile_step(std::integral_constant<int, 1>{}, j, s, s, more, cs1, co1)))
             break;
           mma_commit(bar(bars->pl_empty[s]));
           if (j + 2 == x.nkv) mma_commit(bq_empty);  // the Q K^T just issued was the item's last
@@ -735,11 +724,11 @@ __global__ void __launch_bounds__(kRope ? kRopeThreads : kThreads, 1)
     __syncwarp();
   } else if (kRope && warp >= kRopeWarp0) {
     // ======================= RoPE (warps 10-11, RoPE kernels) ===========
-    // The window-local RoPE of the item's video Q tiles and of every video K
-    // tile, in shared memory between the TMA landing (q_full / pl_full) and
-    // the MMA (q_ready / pl_ready).  Text tiles arrive already rotated; V
-    // tiles pass through.  Same order as the producer, so no phase is ever
-    // more than one ahead of these waits.
+    // The window-local RoPE of the item's video Q tiles, in shared memory
+    // between the TMA landing (q_full) and the MMA (q_ready).  Text Q tiles
+    // arrive already rotated.  The producer loads the next item's Q only
+    // after the MMA's last Q K^T of this one, which follows q_ready, so these
+    // waits are never more than one phase behind.
     const int rt = threadIdx.x - kRopeWarp0 * 32;  // 0..63
     uint2* tab = reinterpret_cast<uint2*>(smem + C::kTab);
     const uint32_t tab_s = base + C::kTab;
@@ -752,7 +741,7 @@ __global__ void __launch_bounds__(kRope ? kRopeThreads : kThreads, 1)
       tab[row * kRopeStride + i] = make_uint2(pack_bf16(cs, cs), pack_bf16(-sn, sn));
     }
     asm volatile("bar.sync 1, 64;" ::: "memory");
-    int e = 0, k = 0;
+    int k = 0;
     bool good = true;
     for (int u = 0; good; ++u, ++k) {
       const int it = take_item(u, good);
@@ -770,15 +759,6 @@ __global__ void __launch_bounds__(kRope ? kRopeThreads : kThreads, 1)
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       mbar_arrive(bar(bars->q_ready));
-      for (int pl = 0; pl <= x.nkv; ++pl, ++e) {
-        const int slot = e & 1;
-        if (!(good = wait_phase(bar(bars->pl_full[slot]), (e >> 1) & 1, abort_flag, p.status))) break;
-        if (pl < x.vt)  // this payload's K tile (K_pl) is a video tile
-          rope_tile(base + C::kK + slot * C::kQKTileBytes, pl * kBN, min(kBN, x.n_w - pl * kBN), bh, bw, p.wt, p.wh, tab_s,
-                    inv_bhw, inv_bw, rt);
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_arrive(bar(bars->pl_ready[slot]));
-      }
     }
   } else {
     // ======================= softmax + epilogue (warps 0-7) =============
@@ -986,7 +966,7 @@ int launch(const AttnCall& c) {
   CUtensorMap mq, mk, mv, mqt, mkt, mvt;
   const int64_t cols = static_cast<int64_t>(c.heads) * HD;
   if (int rc = make_map(&mq, c.q, c.N, cols, c.vid_stride_B, kFp8)) return rc;
-  if (int rc = make_map(&mk, c.k, c.N, cols, c.vid_stride_B, kFp8)) return rc;
+  if (int rc = make_map(&mk, c.k, c.N, cols, c.vid_k_stride_B ? c.vid_k_stride_B : c.vid_stride_B, kFp8)) return rc;
   if (int rc = make_map(&mv, c.v, c.N, cols, c.vid_v_stride_B)) return rc;
   if (c.L > 0) {
     if (int rc = make_map(&mqt, c.qt, c.L, cols, c.txt_stride_B, kFp8)) return rc;

@@ -36,6 +36,8 @@ constexpr int kWarps = 8;
 struct RopeParams {
   char *q, *k, *qt, *kt;
   int64_t stride, tstride;  // bytes
+  char* kdst;               // rope_k_copy_kernel: destination rows (dstride bytes apart)
+  int64_t dstride;
   const int32_t *win_off, *ids, *boxes;
   int nwin, N, L, heads, H, W;
   float theta[kPairsPerAxis];  // base^(-2i/42)
@@ -106,6 +108,33 @@ __device__ __forceinline__ void rotate_rows(char* qrow, char* krow, int heads, c
   }
 }
 
+// The (cos, sin) table of row r (video rows in layout order, then text
+// rows): one warp finds the row's window and window-local position and
+// fills cs[0 .. 62].
+__device__ __forceinline__ void row_table(const RopeParams& p, int64_t r, float2* cs, int lane) {
+  int pos[3];
+  if (r < p.N) {
+    int lo = 0, hi = p.nwin - 1;  // window holding layout row r
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (__ldg(p.win_off + mid) <= r) lo = mid; else hi = mid - 1;
+    }
+    const int c = __ldg(p.ids + r);
+    const int t = c / (p.H * p.W), h = (c / p.W) % p.H, w = c % p.W;
+    const int32_t* box = p.boxes + lo * 6;  // t0,t1,h0,h1,w0,w1
+    pos[0] = p.L + t - __ldg(box + 0);
+    pos[1] = h - __ldg(box + 2);
+    pos[2] = w - __ldg(box + 4);
+  } else {
+    pos[0] = pos[1] = pos[2] = static_cast<int>(r - p.N);
+  }
+  for (int q = lane; q < kPairs; q += 32) {
+    float s, c;
+    sincosf(static_cast<float>(pos[q / kPairsPerAxis]) * p.theta[q % kPairsPerAxis], &s, &c);
+    cs[q] = make_float2(c, s);
+  }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kWarps * 32) rope_kernel(const RopeParams p) {
   __shared__ float2 table[kWarps][kPairs + 1];
@@ -114,32 +143,47 @@ __global__ void __launch_bounds__(kWarps * 32) rope_kernel(const RopeParams p) {
   const int64_t rows = static_cast<int64_t>(p.N) + p.L;
   for (int64_t r = static_cast<int64_t>(blockIdx.x) * kWarps + wib; r < rows;
        r += static_cast<int64_t>(gridDim.x) * kWarps) {
-    int pos[3];
-    if (r < p.N) {
-      int lo = 0, hi = p.nwin - 1;  // window holding layout row r
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (__ldg(p.win_off + mid) <= r) lo = mid; else hi = mid - 1;
-      }
-      const int c = __ldg(p.ids + r);
-      const int t = c / (p.H * p.W), h = (c / p.W) % p.H, w = c % p.W;
-      const int32_t* box = p.boxes + lo * 6;  // t0,t1,h0,h1,w0,w1
-      pos[0] = p.L + t - __ldg(box + 0);
-      pos[1] = h - __ldg(box + 2);
-      pos[2] = w - __ldg(box + 4);
-    } else {
-      pos[0] = pos[1] = pos[2] = static_cast<int>(r - p.N);
-    }
-    for (int q = lane; q < kPairs; q += 32) {
-      float s, c;
-      sincosf(static_cast<float>(pos[q / kPairsPerAxis]) * p.theta[q % kPairsPerAxis], &s, &c);
-      cs[q] = make_float2(c, s);
-    }
+    row_table(p, r, cs, lane);
     __syncwarp();
     if (r < p.N)
       rotate_rows<T>(p.q + r * p.stride, p.k + r * p.stride, p.heads, cs, lane);
     else
       rotate_rows<T>(p.qt + (r - p.N) * p.tstride, p.kt + (r - p.N) * p.tstride, p.heads, cs, lane);
+    __syncwarp();
+  }
+}
+
+// Video k only, rotated out of place (bf16): row r of p.k (stride p.stride)
+// to row r of p.kdst (stride p.dstride), 2 * kBatch chunks per lane in
+// flight like rope_kernel's q and k.
+__global__ void __launch_bounds__(kWarps * 32) rope_k_copy_kernel(const RopeParams p) {
+  __shared__ float2 table[kWarps][kPairs + 1];
+  const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float2* cs = table[wib];
+  constexpr int kPer = 8, kB = 2 * kBatch;
+  const int chunks = p.heads * kHd / kPer;
+  for (int64_t r = static_cast<int64_t>(blockIdx.x) * kWarps + wib; r < p.N;
+       r += static_cast<int64_t>(gridDim.x) * kWarps) {
+    row_table(p, r, cs, lane);
+    __syncwarp();
+    const char* src = p.k + r * p.stride;
+    char* dst = p.kdst + r * p.dstride;
+    for (int c0 = 0; c0 < chunks; c0 += 32 * kB) {
+      int4 a[kB];
+#pragma unroll
+      for (int u = 0; u < kB; ++u) {
+        const int c = c0 + u * 32 + lane;
+        if (c < chunks) a[u] = __ldg(reinterpret_cast<const int4*>(src + static_cast<int64_t>(c) * 16));
+      }
+#pragma unroll
+      for (int u = 0; u < kB; ++u) {
+        const int c = c0 + u * 32 + lane;
+        if (c < chunks) {
+          rotate_chunk<__nv_bfloat16>(a[u], c, cs);
+          *reinterpret_cast<int4*>(dst + static_cast<int64_t>(c) * 16) = a[u];
+        }
+      }
+    }
     __syncwarp();
   }
 }
@@ -174,6 +218,33 @@ int rope_text_copy(const void* qt, const void* kt, int64_t txt_stride_B, void* q
   const unsigned blocks = static_cast<unsigned>((L + kWarps - 1) / kWarps);
   rope_kernel<__nv_bfloat16><<<blocks, kWarps * 32, 0, stream>>>(p);
   return cuda_check(cudaGetLastError(), "rope_kernel launch (text)");
+}
+
+int rope_k_copy(const wp_plan* plan, int layout, const void* k, int64_t vid_stride_B, void* k_out, int heads, int L,
+                float rope_base, cudaStream_t stream) {
+  if (plan->N == 0) return WP_OK;
+  RopeParams p{};
+  p.k = static_cast<char*>(const_cast<void*>(k));
+  p.stride = vid_stride_B;
+  p.kdst = static_cast<char*>(k_out);
+  p.dstride = static_cast<int64_t>(heads) * kHd * 2;
+  p.win_off = dev_ptr<int32_t>(plan, plan->dlay[layout].win_off);
+  p.ids = dev_ptr<int32_t>(plan, plan->dlay[layout].ids);
+  p.boxes = dev_ptr<int32_t>(plan, plan->dlay[layout].boxes);
+  p.nwin = plan->lay[layout].nwin;
+  p.N = static_cast<int>(plan->N);
+  p.L = L;  // positions only: video t offset by L
+  p.heads = heads;
+  p.H = plan->H;
+  p.W = plan->W;
+  rope_theta(rope_base, p.theta);
+  int sms = 0;
+  if (int rc = cuda_check(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, plan->device),
+                          "cudaDeviceGetAttribute"))
+    return rc;
+  const int64_t blocks = std::min<int64_t>((plan->N + kWarps - 1) / kWarps, static_cast<int64_t>(sms) * 8);
+  rope_k_copy_kernel<<<static_cast<unsigned>(blocks), kWarps * 32, 0, stream>>>(p);
+  return cuda_check(cudaGetLastError(), "rope_k_copy_kernel launch");
 }
 
 }  // namespace wp

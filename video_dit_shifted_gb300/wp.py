@@ -241,9 +241,10 @@ def make_workspace(plan, layout, heads, head_dim, L, dtype_code, device, rope=Fa
 def window_attn_rope(plan, layout, q, k, v, qt, kt, vt, o_vid, o_txt, workspace, rope_base=10000.0,
                      scale=0.0, stream=None, out_layout=CANONICAL):
     """Window attention on un-rotated q, k with the window-local RoPE applied
-    inside the kernel (wp_window_attn_rope in include/wp.h); q, k, qt, kt are
-    not modified.  Arguments as window_attn; workspace from
-    make_workspace(..., rope=True)."""
+    within the call (wp_window_attn_rope in include/wp.h: k and the text q/k
+    rotated once into the workspace, video Q tiles inside the attention
+    kernel); q, k, qt, kt are not modified.  Arguments as window_attn;
+    workspace from make_workspace(..., rope=True)."""
     N, heads, hd = q.shape
     L = qt.shape[0] if qt is not None else 0
     es = q.element_size()
