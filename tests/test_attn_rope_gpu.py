@@ -1,9 +1,10 @@
 """wp_window_attn_rope (window attention with the window-local RoPE applied
-inside the kernel) against the oracle's RoPE followed by the oracle's window
-attention (gpu).
+within the call: k rotated once into the workspace, the video Q tiles inside
+the attention kernel) against the oracle's RoPE followed by the oracle's
+window attention (gpu).
 
 Tolerance: bf16, max abs error <= 2e-2 against the float64 oracle fed the same
-un-rotated input bits (the kernel rotates in bf16 arithmetic)."""
+un-rotated input bits (Q is rotated in bf16 arithmetic)."""
 import numpy as np
 import pytest
 import torch
@@ -93,6 +94,39 @@ def test_rope_attention_agrees_with_rope_pass(vds):
                             out_layout=out_layout)
             assert (o1.float() - o2.float()).abs().max().item() <= TOL
             assert (t1.float() - t2.float()).abs().max().item() <= TOL
+    plan.close()
+
+
+@pytest.mark.parametrize("layout", [op.REGULAR, op.SHIFTED])
+def test_rope_attention_rotated_k_equals_rope_pass(vds, layout):
+    """The call rotates k once into its workspace (documented layout: after
+    the status block, the T_w partials and the rotated text q/k, from the
+    next multiple of 1024 bytes, [N, heads, 128] bf16).  Both that pass and
+    wp_rope rotate in fp32 and round once, so the copy equals wp_rope's k bit
+    for bit; k itself is left as it was.  q/k come packed with v, as a
+    projection writes them (row stride 3 * heads * 256 bytes)."""
+    from video_dit_shifted_gb300 import synth
+    grid, heads, L = (3, 30, 40, 2, 3, 3), 3, 200
+    plan = vds.Plan(*grid, device="cuda")
+    N = plan.N
+    g = torch.Generator(device="cuda").manual_seed(11 + layout)
+    qkv = torch.randn((N, 3, heads, 128), device="cuda", generator=g).to(torch.bfloat16)
+    x = synth.attention_inputs(N, L, heads, 128, torch.bfloat16, "cuda", base_seed=5)
+    k_before = qkv[:, 1].clone()
+    o = torch.empty((N, heads, 128), dtype=torch.bfloat16, device="cuda")
+    t = torch.empty((L, heads, 128), dtype=torch.bfloat16, device="cuda")
+    ws = vds.make_workspace(plan, layout, heads, 128, L, vds.BF16, "cuda", rope=True)
+    vds.window_attn_rope(plan, layout, qkv[:, 0], qkv[:, 1], qkv[:, 2], x["qt"], x["kt"], x["vt"], o, t, ws)
+    assert vds.read_status(ws) == 0
+    assert torch.equal(qkv[:, 1], k_before)
+    plain = vds.wp.workspace_bytes(plan, layout, heads, 128, L, vds.BF16)
+    off = (plain + 2 * L * heads * 128 * 2 + 1023) // 1024 * 1024
+    assert ws.numel() == off + N * heads * 128 * 2
+    krot = ws[off:].view(torch.bfloat16).view(N, heads, 128)
+    ref = qkv.clone()
+    vds.rope(plan, layout, ref[:, 0], ref[:, 1], x["qt"].clone(), x["kt"].clone())
+    torch.cuda.synchronize()
+    assert torch.equal(krot, ref[:, 1])
     plan.close()
 
 
