@@ -1,7 +1,8 @@
 """CPU model of the persistent attention kernel's barrier protocol.
 
 The kernel (csrc/attn_tc.cu) coordinates a TMA producer, an MMA-issuing
-warp, two softmax warpgroups (and, in the RoPE kernels, two rotating warps)
+warp, two softmax warpgroups (and, in the RoPE kernels, two warps that
+rotate each item's Q tiles between the TMA landing and the MMA)
 through mbarriers that are waited on by phase parity; work items reach all
 roles through a ring of four slots filled from a global counter.  This model replays each role's sequence of waits, arrivals
 and commits (a commit arrives when the MMAs before it finish; here, at once)
@@ -65,7 +66,7 @@ def counts(rope):
     stand for whole warps or warpgroups, one arrival each)."""
     c = {b: 1 for b in ('q_full', 'q_empty', 'pl_full0', 'pl_full1', 'pl_empty0', 'pl_empty1',
                         's_full0', 's_full1', 'p_full0', 'p_full1', 'o_full0', 'o_full1',
-                        'o_empty0', 'o_empty1', 'q_ready', 'pl_ready0', 'pl_ready1')}
+                        'o_empty0', 'o_empty1', 'q_ready')}
     for u in range(NRING):
         c['item_full%d' % u] = 1
         c['item_empty%d' % u] = 4 if rope else 3    # MMA, two softmax warpgroups (+ RoPE warps)
@@ -105,8 +106,8 @@ def mma(src, rope):
         item = src.get(u)
         if item is None: break
         (w, h, nkv, nq, t0, vt) = item
-        yield ('wait','q_ready' if rope else 'q_full',k)
-        yield ('wait',('pl_ready%d' if rope else 'pl_full%d')%(e&1),e>>1)   # payload [K(0)]
+        yield ('wait','q_ready' if rope else 'q_full',k)     # RoPE kernels: Q rotated
+        yield ('wait','pl_full%d'%(e&1),e>>1)                # payload [K(0)]
         for i in range(nq): yield ('commit','s_full%d'%i)
         if nkv==1: yield ('commit','q_empty')
         yield ('commit','pl_empty%d'%(e&1))            # K(0) read by the S(0) just issued
@@ -117,9 +118,7 @@ def mma(src, rope):
             for i in range(nq):
                 yield ('wait','p_full%d'%i,cs[i]+j)
                 if j==0 and co[i]>0: yield ('wait','o_empty%d'%i,co[i]-1)
-                if rope and more and i == 0: yield ('wait','pl_ready%d'%(e&1),e>>1)   # rotated K(j+1)
                 yield ('commit',('s_full%d' if more else 'o_full%d')%i)
-            if rope and not more: yield ('wait','pl_ready%d'%(e&1),e>>1)   # RoPE warps passed it
             yield ('commit','pl_empty%d'%(e&1))        # V(j) and K(j+1) read by MMAs just issued
             if j+2==nkv: yield ('commit','q_empty')
             e+=1
@@ -142,19 +141,14 @@ def softmax(src,i):
         yield ('arrive','o_empty%d'%i); co+=1
 
 def rope_warps(src):
-    # RoPE kernels: rotate the item's Q and every payload's K between the TMA
-    # landing and the MMA.
-    e=0; k=0
+    # RoPE kernels: rotate the item's Q tiles between the TMA landing and the
+    # MMA (K arrives rotated; K/V payloads go from the TMA to the MMA).
+    k=0
     for u in range(1 << 30):
         yield from take(u)
         item = src.get(u)
         if item is None: break
-        (w, h, nkv, nq, t0, vt) = item
         yield ('wait','q_full',k); yield ('arrive','q_ready'); k+=1
-        for p in range(nkv+1):
-            yield ('wait','pl_full%d'%(e&1),e>>1)
-            yield ('arrive','pl_ready%d'%(e&1))
-            e+=1
 
 def simulate(items, seed, rope=False, lag=None):
     """Random interleaving; a role index in `lag` is picked only when nothing
@@ -212,25 +206,20 @@ def test_protocol_has_no_deadlock_and_exact_parity(grid, L, heads, nb, layout, r
                 simulate(its, seed, rope, lag=lag)
 
 
-def test_model_catches_an_early_release():
-    """The checker itself: with the RoPE warps, an MMA that released an item's
-    last (V-only) payload without waiting for pl_ready lets the producer
-    refill the slot while the RoPE warps are still a payload behind; the
-    model must flag that (a parity wait that aliases, or a deadlock)."""
+def test_model_catches_an_unrotated_q():
+    """The checker itself: in the RoPE kernels an MMA that started an item on
+    the landed Q (q_full) instead of the rotated one (q_ready) would let the
+    producer reload the Q tiles while the rotating warps are still an item
+    behind; the model must flag that (a parity wait that aliases, or a
+    deadlock)."""
     its = items_for((3, 30, 40, 2, 3, 3), 0, 2, 3, 1, op.SHIFTED)
     global mma
     good_mma = mma
 
-    def early_release(src, rope):
-        ops = list(good_mma(src, rope))
-        out = []
-        for n, op_ in enumerate(ops):
-            if (op_[0] == 'wait' and op_[1].startswith('pl_ready') and n + 1 < len(ops)
-                    and ops[n + 1][0] == 'commit' and ops[n + 1][1].startswith('pl_empty')):
-                continue
-            out.append(op_)
-        yield from out
-    mma = early_release
+    def unrotated(src, rope):
+        for op_ in good_mma(src, rope):
+            yield ('wait', 'q_full', op_[2]) if op_[:2] == ('wait', 'q_ready') else op_
+    mma = unrotated
     try:
         with pytest.raises((AssertionError, RuntimeError)):
             for seed in range(200):
