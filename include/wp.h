@@ -79,13 +79,23 @@ enum wp_status {
  *   to even), wt = ceil(min(T, 30)/nt).
  * Regular intervals per axis are [i*w, min((i+1)*w, n)).  Shifted intervals
  * cut at floor((2k+1)*w/2) (half window, floored -- a reading: the page does
- * not say how an odd half is rounded) clipped to [0, n]; an axis a single
- * window already covers is not shifted.  Windows are enumerated w outermost,
+ * not say how an odd half is rounded; wp_plan_create_ex takes the other)
+ * clipped to [0, n]; an axis a single window already covers is not
+ * shifted.  Windows are enumerated w outermost,
  * then h, then t.  All host work; no CUDA call.
  * Errors: WP_EINVAL if any argument < 1, T*H*W >= 2^31, or a window
  * dimension comes out as 0.  *out is set only on success; free it with
  * wp_plan_destroy. */
 int wp_plan_create(int T, int H, int W, int nt, int nh, int nw, wp_plan** out);
+
+/* wp_plan_create_ex -- wp_plan_create with options.  flags = 0 is
+ * wp_plan_create; WP_PLAN_HALF_CEIL rounds an odd half window up instead:
+ * shifted cuts at ceil((2k+1)*w/2) (w = 15: 8, 23, 38, ... instead of 7,
+ * 22, 37, ...), the other reading of "moved by half a window" that the page
+ * leaves open.  Regular layouts and even window sizes are the same either
+ * way.  WP_EINVAL also for unknown flag bits. */
+#define WP_PLAN_HALF_CEIL 1u
+int wp_plan_create_ex(int T, int H, int W, int nt, int nh, int nw, unsigned flags, wp_plan** out);
 void wp_plan_destroy(wp_plan* plan); /* NULL is a no-op */
 
 /* Geometry of one layout.  n_tokens = T*H*W; nwin = window count (1 for

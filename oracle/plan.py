@@ -17,9 +17,10 @@ Follows "Window-Aligned Sequence Parallelism (SeedVR2)", §Window layouts:
 Readings of points the page leaves open:
 
 * ``round`` is Python's ``round`` on the float64 product (ties to even).
-* The half-window shift of an odd window length is floored: cuts sit at
-  ``floor((2k+1)*w/2)``.  PARITY UNPINNED: ceil would also partition the grid,
-  so no invariant on the pages distinguishes the two.
+* The half-window shift of an odd window length is floored by default: cuts
+  sit at ``floor((2k+1)*w/2)``; ``half="ceil"`` takes the other reading,
+  ``ceil((2k+1)*w/2)``.  PARITY UNPINNED: both partition the grid, so no
+  invariant on the pages distinguishes the two.
 * An axis that a single window already covers (``w >= n``) has no interior cut
   to move, so its shifted interval list is the single interval ``[0, n)``.
 """
@@ -52,20 +53,27 @@ def regular_intervals(n, w):
     return [(i * w, min((i + 1) * w, n)) for i in range(_ceil_div(n, w))]
 
 
-def shifted_intervals(n, w):
-    """Cuts moved by half a window (floored), clipped to [0, n]."""
+def shifted_intervals(n, w, half="floor"):
+    """Cuts moved by half a window, clipped to [0, n].  The cut after the
+    k-th regular window moves to (k + 1/2) * w; for an odd w that is not an
+    integer and the page does not say which way it goes: half="floor" (the
+    default) takes floor, half="ceil" takes ceil."""
     if w >= n:
         return [(0, n)]
     cuts = {0, n}
     k = 0
-    while (2 * k + 1) * w // 2 < n:
-        cuts.add((2 * k + 1) * w // 2)
+    while True:
+        num = (2 * k + 1) * w                      # the cut is num / 2
+        cut = num // 2 if half == "floor" else -(-num // 2)
+        if cut >= n:
+            break
+        cuts.add(cut)
         k += 1
     cuts = sorted(cuts)
     return [(a, b) for a, b in zip(cuts[:-1], cuts[1:])]
 
 
-def layout_boxes(T, H, W, nt, nh, nw, layout):
+def layout_boxes(T, H, W, nt, nh, nw, layout, half="floor"):
     """Window boxes ((t0,t1),(h0,h1),(w0,w1)) in enumeration order.
 
     CANONICAL is one box covering the grid, so its token order is row-major
@@ -74,7 +82,10 @@ def layout_boxes(T, H, W, nt, nh, nw, layout):
     if layout == CANONICAL:
         return [((0, T), (0, H), (0, W))]
     wt, wh, ww = window_size(T, H, W, nt, nh, nw)
-    axis = regular_intervals if layout == REGULAR else shifted_intervals
+    if layout == REGULAR:
+        axis = regular_intervals
+    else:
+        axis = lambda n, w: shifted_intervals(n, w, half)
     ti, hi, wi = axis(T, wt), axis(H, wh), axis(W, ww)
     boxes = []
     for iw in wi:            # w outermost
@@ -84,14 +95,14 @@ def layout_boxes(T, H, W, nt, nh, nw, layout):
     return boxes
 
 
-def layout_tables(T, H, W, nt, nh, nw, layout):
+def layout_tables(T, H, W, nt, nh, nw, layout, half="floor"):
     """(win_off, ids): window offsets and layout-position -> canonical id.
 
     ids is obtained by windowing arange(T*H*W).reshape(T, H, W) box by box.
     """
     cube = np.arange(T * H * W, dtype=np.int64).reshape(T, H, W)
     pieces, off = [], [0]
-    for (t0, t1), (h0, h1), (w0, w1) in layout_boxes(T, H, W, nt, nh, nw, layout):
+    for (t0, t1), (h0, h1), (w0, w1) in layout_boxes(T, H, W, nt, nh, nw, layout, half):
         piece = cube[t0:t1, h0:h1, w0:w1].reshape(-1)
         pieces.append(piece)
         off.append(off[-1] + piece.size)

@@ -23,10 +23,11 @@ import numpy as np
 from . import plan as op
 
 
-def positions(T, H, W, nt, nh, nw, layout, L):
-    """(pos_video [N, 3] in layout row order, pos_text [L, 3])."""
+def positions(T, H, W, nt, nh, nw, layout, L, half="floor"):
+    """(pos_video [N, 3] in layout row order, pos_text [L, 3]); half as in
+    plan.layout_boxes."""
     rows = []
-    for (t0, t1), (h0, h1), (w0, w1) in op.layout_boxes(T, H, W, nt, nh, nw, layout):
+    for (t0, t1), (h0, h1), (w0, w1) in op.layout_boxes(T, H, W, nt, nh, nw, layout, half):
         for t in range(t0, t1):          # row-major (t, h, w) inside a window
             for h in range(h0, h1):
                 for w in range(w0, w1):

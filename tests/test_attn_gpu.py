@@ -40,14 +40,14 @@ def _run(vds, plan, layout, x, heads, hd, L, dtype, scale=0.0):
     return o_vid, o_txt, ws
 
 
-def _check_full(vds, grid, heads, hd, L, dtype, layouts=(op.REGULAR, op.SHIFTED), scale=0.0):
+def _check_full(vds, grid, heads, hd, L, dtype, layouts=(op.REGULAR, op.SHIFTED), scale=0.0, half="floor"):
     from video_dit_shifted_gb300 import synth
-    plan = vds.Plan(*grid, device="cuda")
+    plan = vds.Plan(*grid, device="cuda", half=half)
     N = plan.N
     for layout in layouts:
         x = synth.attention_inputs(N, L, heads, hd, dtype, "cuda", base_seed=10 * layout)
         o_vid, o_txt, _ = _run(vds, plan, layout, x, heads, hd, L, dtype, scale)
-        off, ids = op.layout_tables(*grid, layout)
+        off, ids = op.layout_tables(*grid, layout, half=half)
         ref_o, ref_t = oa.window_attention(*(_np(x[n]) for n in ("q", "k", "v", "qt", "kt", "vt")), off, ids,
                                            scale=scale if scale > 0 else None)
         err_v = np.abs(_np(o_vid) - ref_o).max()
@@ -83,6 +83,24 @@ def test_single_window_is_global_attention(vds):
     """One window covers the grid: global attention over [video ; text]."""
     _check_full(vds, (3, 9, 16, 1, 1, 1), 2, 128, 7, torch.bfloat16)
     _check_full(vds, (3, 9, 16, 1, 1, 1), 2, 64, 7, torch.float32)
+
+
+@pytest.mark.parametrize("dtype,hd", [(torch.bfloat16, 128), (torch.float32, 64)])
+def test_half_ceil_plan(vds, dtype, hd):
+    """A plan made with the other reading of an odd half window
+    (WP_PLAN_HALF_CEIL) against the oracle's half="ceil" windows: attention
+    in both layouts, and the re-layout between them bit for bit."""
+    from oracle import permute as opm
+    grid = (2, 45, 80, 1, 3, 3)           # window 2 x 15 x 27: odd on both spatial axes
+    _check_full(vds, grid, 2, hd, 40, dtype, half="ceil")
+    plan = vds.Plan(*grid, device="cuda", half="ceil")
+    rows = torch.randint(-2 ** 15, 2 ** 15, (plan.N, 48), dtype=torch.int16, device="cuda")
+    out = torch.empty_like(rows)
+    vds.permute(plan, rows, out, vds.REGULAR, vds.SHIFTED)
+    torch.cuda.synchronize()
+    ids = {l: op.layout_tables(*grid, l, half="ceil")[1] for l in (op.REGULAR, op.SHIFTED)}
+    assert np.array_equal(out.cpu().numpy(), opm.permute_rows(rows.cpu().numpy(), ids[op.REGULAR], ids[op.SHIFTED]))
+    plan.close()
 
 
 def test_custom_scale(vds):

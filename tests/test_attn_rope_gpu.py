@@ -30,11 +30,11 @@ def _np(t):
     return t.float().cpu().numpy().astype(np.float64)
 
 
-def _oracle(grid, layout, raw, L, base=10000.0):
-    pv, pt = orp.positions(*grid, layout, L)
+def _oracle(grid, layout, raw, L, base=10000.0, half="floor"):
+    pv, pt = orp.positions(*grid, layout, L, half=half)
     q, k = orp.rope(raw["q"], pv, base), orp.rope(raw["k"], pv, base)
     qt, kt = (orp.rope(raw["qt"], pt, base), orp.rope(raw["kt"], pt, base)) if L else (raw["qt"], raw["kt"])
-    off, ids = op.layout_tables(*grid, layout)
+    off, ids = op.layout_tables(*grid, layout, half=half)
     ref_o, ref_t = oa.window_attention(q, k, raw["v"], qt, kt, raw["vt"], off, ids)
     return ref_o, (oa.text_mean(ref_t) if L else None)
 
@@ -67,6 +67,28 @@ def test_rope_attention_matches_oracle(vds, grid, heads, L):
             assert np.abs(_np(t[:L]) - ref_t).max() <= TOL, layout
         for n, b in before.items():          # the inputs are not rotated in place
             assert torch.equal(x[n], b), n
+    plan.close()
+
+
+def test_rope_attention_half_ceil_plan(vds):
+    """A plan with the other reading of an odd half window (window 2 x 15 x
+    27; WP_PLAN_HALF_CEIL): the window-local positions follow the plan's
+    boxes, against the oracle's half="ceil" windows and positions."""
+    from video_dit_shifted_gb300 import synth
+    grid, heads, L = (2, 45, 80, 1, 3, 3), 2, 16
+    plan = vds.Plan(*grid, device="cuda", half="ceil")
+    N = plan.N
+    for layout in (op.REGULAR, op.SHIFTED):
+        x = synth.attention_inputs(N, L, heads, 128, torch.bfloat16, "cuda", base_seed=9 + layout)
+        raw = {n: _np(x[n]) for n in ("q", "k", "v", "qt", "kt", "vt")}
+        o = torch.full((N, heads, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+        t = torch.full((L, heads, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+        ws = vds.make_workspace(plan, layout, heads, 128, L, vds.BF16, "cuda", rope=True)
+        vds.window_attn_rope(plan, layout, x["q"], x["k"], x["v"], x["qt"], x["kt"], x["vt"], o, t, ws)
+        assert vds.read_status(ws) == 0
+        ref_o, ref_t = _oracle(grid, layout, raw, L, half="ceil")
+        assert np.abs(_np(o) - ref_o).max() <= TOL, layout
+        assert np.abs(_np(t) - ref_t).max() <= TOL, layout
     plan.close()
 
 

@@ -31,8 +31,10 @@ def test_intervals_golden(golden):
     rows = golden("intervals.txt")
     for r in rows:
         kind, n, w = r[0], int(r[1]), int(r[2])
-        fn = op.regular_intervals if kind == "regular" else op.shifted_intervals
+        fn = {"regular": op.regular_intervals, "shifted": op.shifted_intervals,
+              "shifted_ceil": lambda n, w: op.shifted_intervals(n, w, half="ceil")}[kind]
         assert fn(n, w) == _parse_intervals(r[3:]), r
+    assert {r[0] for r in rows} == {"regular", "shifted", "shifted_ceil"}
 
 
 def _layout(name):
@@ -53,13 +55,16 @@ def test_window_tokens_pr1_golden(golden):
         assert np.diff(off).tolist() == list(map(int, r[1:])), r
 
 
-def _brute_force_ids(T, H, W, nt, nh, nw, layout):
+def _brute_force_ids(T, H, W, nt, nh, nw, layout, half="floor"):
     """Layout order from scratch: for every token find the window that holds
     it by scanning the per-axis intervals, then order tokens by
     (window index in w->h->t enumeration, canonical id).  Within a box,
     row-major (t,h,w) order is increasing canonical id."""
     wt, wh, ww = op.window_size(T, H, W, nt, nh, nw)
-    ax = op.regular_intervals if layout == op.REGULAR else op.shifted_intervals
+    if layout == op.REGULAR:
+        ax = op.regular_intervals
+    else:
+        ax = lambda n, w: op.shifted_intervals(n, w, half)
     ti, hi, wi = ax(T, wt), ax(H, wh), ax(W, ww)
 
     def find(ints, x):
@@ -89,10 +94,10 @@ SMALL_GRIDS = [
 
 
 @pytest.mark.parametrize("grid", SMALL_GRIDS)
-@pytest.mark.parametrize("layout", [op.REGULAR, op.SHIFTED])
-def test_ids_match_brute_force(grid, layout):
-    off, ids = op.layout_tables(*grid, layout)
-    assert np.array_equal(ids, _brute_force_ids(*grid, layout))
+@pytest.mark.parametrize("layout,half", [(op.REGULAR, "floor"), (op.SHIFTED, "floor"), (op.SHIFTED, "ceil")])
+def test_ids_match_brute_force(grid, layout, half):
+    off, ids = op.layout_tables(*grid, layout, half=half)
+    assert np.array_equal(ids, _brute_force_ids(*grid, layout, half))
     assert off[0] == 0 and off[-1] == ids.size
 
 
@@ -114,8 +119,8 @@ def test_layouts_partition_the_grid(grid):
     wt, wh, ww = op.window_size(*grid)
     if min(wt, wh, ww) <= 0:
         pytest.skip("window of size 0 (rejected by the planner)")
-    for layout in (op.REGULAR, op.SHIFTED):
-        off, ids = op.layout_tables(*grid, layout)
+    for layout, half in ((op.REGULAR, "floor"), (op.SHIFTED, "floor"), (op.SHIFTED, "ceil")):
+        off, ids = op.layout_tables(*grid, layout, half=half)
         assert np.array_equal(np.sort(ids), np.arange(T * H * W))
         assert np.all(np.diff(off) > 0)  # no empty window
 

@@ -39,15 +39,15 @@ std::vector<Interval> regular_axis(int n, int w) {
   return v;
 }
 
-// Interior cuts at floor((2k+1)*w/2) < n, i.e. every regular cut moved by
-// half a window (odd halves floored) and the ends clipped to 0 and n.  An
+// Interior cuts at floor((2k+1)*w/2) < n (ceil with half_ceil), i.e. every
+// regular cut moved by half a window and the ends clipped to 0 and n.  An
 // axis that one window covers keeps its single interval.
-std::vector<Interval> shifted_axis(int n, int w) {
+std::vector<Interval> shifted_axis(int n, int w, bool half_ceil) {
   if (w >= n) return {{0, n}};
   std::vector<Interval> v;
   int start = 0;
   for (int64_t k = 0;; ++k) {
-    const int64_t cut = ((2 * k + 1) * static_cast<int64_t>(w)) / 2;
+    const int64_t cut = ((2 * k + 1) * static_cast<int64_t>(w) + (half_ceil ? 1 : 0)) / 2;
     if (cut >= n) break;
     if (cut > start) {
       v.push_back({start, static_cast<int>(cut)});
@@ -70,9 +70,10 @@ void build_layout(wp_plan* p, int layout) {
     hi = regular_axis(p->H, p->wh);
     wi = regular_axis(p->W, p->ww);
   } else {
-    ti = shifted_axis(p->T, p->wt);
-    hi = shifted_axis(p->H, p->wh);
-    wi = shifted_axis(p->W, p->ww);
+    const bool up = (p->flags & WP_PLAN_HALF_CEIL) != 0;
+    ti = shifted_axis(p->T, p->wt, up);
+    hi = shifted_axis(p->H, p->wh, up);
+    wi = shifted_axis(p->W, p->ww, up);
   }
   L.nwin = static_cast<int>(ti.size() * hi.size() * wi.size());
   L.win_off.assign(L.nwin + 1, 0);
@@ -183,7 +184,12 @@ const char* wp_last_error(void) { return g_err.c_str(); }
 int wp_abi_version(void) { return WP_ABI_VERSION; }
 
 int wp_plan_create(int T, int H, int W, int nt, int nh, int nw, wp_plan** out) {
+  return wp_plan_create_ex(T, H, W, nt, nh, nw, 0u, out);
+}
+
+int wp_plan_create_ex(int T, int H, int W, int nt, int nh, int nw, unsigned flags, wp_plan** out) {
   if (!out) return fail(WP_EINVAL, "out is NULL");
+  if (flags & ~WP_PLAN_HALF_CEIL) return fail(WP_EINVAL, "unknown plan flags 0x%x", flags);
   if (T < 1 || H < 1 || W < 1 || nt < 1 || nh < 1 || nw < 1)
     return fail(WP_EINVAL, "grid and window counts must be >= 1 (T=%d H=%d W=%d nt=%d nh=%d nw=%d)",
                 T, H, W, nt, nh, nw);
@@ -200,6 +206,7 @@ int wp_plan_create(int T, int H, int W, int nt, int nh, int nw, wp_plan** out) {
   if (!p) return fail(WP_EINVAL, "out of host memory");
   p->T = T; p->H = H; p->W = W; p->nt = nt; p->nh = nh; p->nw = nw;
   p->N = N;
+  p->flags = flags;
   p->wh = static_cast<int>(ceil_div(static_cast<int64_t>(rh), nh));
   p->ww = static_cast<int>(ceil_div(static_cast<int64_t>(rw), nw));
   p->wt = static_cast<int>(ceil_div(std::min(T, kMaxTemporalWindow), nt));

@@ -47,6 +47,7 @@ struct wp_plan {
   int T = 0, H = 0, W = 0, nt = 0, nh = 0, nw = 0;
   int wt = 0, wh = 0, ww = 0;
   int64_t N = 0;
+  unsigned flags = 0;  // WP_PLAN_HALF_CEIL
   wp::LayoutTables lay[wp::kNumLayouts];
   // device side (valid once uploaded)
   wp::DeviceLayout dlay[wp::kNumLayouts];

@@ -12,6 +12,7 @@ import torch
 
 CANONICAL, REGULAR, SHIFTED = 0, 1, 2
 BF16, FP32 = 0, 1
+PLAN_HALF_CEIL = 1  # WP_PLAN_HALF_CEIL
 STATUS_NAMES = {0: "WP_OK", 1: "WP_EINVAL", 2: "WP_EUNSUPPORTED", 3: "WP_ECUDA",
                 4: "WP_ETIMEOUT", 5: "WP_EDEVICE", 6: "WP_ENOTREADY"}
 
@@ -24,6 +25,7 @@ _pi32 = ctypes.POINTER(ctypes.c_int32)
 # name -> (restype, argtypes); mirrors include/wp.h
 SIGNATURES = {
     "wp_plan_create": (_c_int, [_c_int] * 6 + [ctypes.POINTER(_vp)]),
+    "wp_plan_create_ex": (_c_int, [_c_int] * 6 + [ctypes.c_uint, ctypes.POINTER(_vp)]),
     "wp_plan_destroy": (None, [_vp]),
     "wp_plan_info": (_c_int, [_vp, _c_int, ctypes.POINTER(_c_i64)] + [ctypes.POINTER(_c_int)] * 5),
     "wp_plan_host_tables": (_c_int, [_vp, _c_int, _pi32, _pi32, _pi32]),
@@ -101,10 +103,16 @@ def _ptr(t):
 class Plan:
     """Window geometry of one (T, H, W) grid; optionally uploaded to a GPU."""
 
-    def __init__(self, T, H, W, nt, nh, nw, device=None, stream=None):
+    def __init__(self, T, H, W, nt, nh, nw, device=None, stream=None, half="floor"):
+        """half: how an odd half window is rounded in the shifted layout,
+        "floor" (the default) or "ceil" (wp_plan_create_ex in include/wp.h)."""
+        if half not in ("floor", "ceil"):
+            raise ValueError("half must be 'floor' or 'ceil'")
         h = ctypes.c_void_p()
-        _check("wp_plan_create", lib().wp_plan_create(T, H, W, nt, nh, nw, ctypes.byref(h)))
+        flags = PLAN_HALF_CEIL if half == "ceil" else 0
+        _check("wp_plan_create_ex", lib().wp_plan_create_ex(T, H, W, nt, nh, nw, flags, ctypes.byref(h)))
         self._h = h
+        self.half = half
         self.T, self.H, self.W, self.nt, self.nh, self.nw = T, H, W, nt, nh, nw
         self.N = T * H * W
         self.dev_buf = None
