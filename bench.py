@@ -249,13 +249,18 @@ def run_e2e(wl, steps, warmup):
     for e in out_done:
         e.record(torch.cuda.current_stream())
 
-    def one(i):
+    copy_ev = []  # per step: (h2d start, h2d end, d2h start, d2h end), timing events
+
+    def one(i, timed=False):
         b = i % nsets
         w = sets[b]
+        ev4 = [torch.cuda.Event(enable_timing=True) for _ in range(4)] if timed else None
         s_in.wait_event(out_done[b])           # this set's last outputs (and so its compute) are done
         with torch.cuda.stream(s_in):
+            if timed: ev4[0].record(s_in)
             for k, dst in ins(w).items():
                 dst.copy_(pinned_in[k], non_blocking=True)
+            if timed: ev4[1].record(s_in)
             in_done[b].record(s_in)
         s_comp.wait_event(in_done[b])
         with torch.cuda.stream(s_comp):
@@ -265,9 +270,12 @@ def run_e2e(wl, steps, warmup):
             comp_done[b].record(s_comp)
         s_out.wait_event(comp_done[b])
         with torch.cuda.stream(s_out):
+            if timed: ev4[2].record(s_out)
             for o, p in zip(outs(w), pinned_out[b]):
                 p.copy_(o, non_blocking=True)
+            if timed: ev4[3].record(s_out)
             out_done[b].record(s_out)
+        if timed: copy_ev.append(ev4)
 
     def copies_only():
         """The same copies with no compute, both directions at once, every
@@ -298,7 +306,7 @@ def run_e2e(wl, steps, warmup):
     s_comp.wait_stream(s_in)
     s_out.wait_stream(s_in)
     for i in range(steps):
-        one(i)
+        one(i, timed=True)
     s_out.wait_stream(s_comp)
     s_out.wait_stream(s_in)
     end.record(s_out)
@@ -306,9 +314,12 @@ def run_e2e(wl, steps, warmup):
     for w in sets:
         w.check_status()
     e2e_ms = start.elapsed_time(end) / steps
+    # The link during the loop: each step's copies in and out, timed on their streams.
+    h2d_ms = statistics.median(e[0].elapsed_time(e[1]) for e in copy_ev)
+    d2h_ms = statistics.median(e[2].elapsed_time(e[3]) for e in copy_ev)
     link_after = copies_only()
     del sets[1:]
-    return e2e_ms, h2d, d2h, (link_before, link_after)
+    return e2e_ms, h2d, d2h, (link_before, link_after), (h2d_ms, d2h_ms)
 
 
 def oracle_sample(wl_name, budget_s, seed_rows=None):
@@ -686,13 +697,18 @@ def run_ours(args):
                 "traffic": recorded_traffic("permute.cu", "permute_1080p") if args.workload == "1080p" else None,
                 "kernel": "permute_rows_kernel", "bytes_per_launch": wl.relayout_bytes, "ms": perm_ms,
                 "peak_source": peak_src}
-    e2e_ms, h2d, d2h, link_ms = run_e2e(wl, args.e2e_steps, max(3, min(args.warmup, 4)))
+    e2e_ms, h2d, d2h, link_ms, loop_copy_ms = run_e2e(wl, args.e2e_steps, max(3, min(args.warmup, 4)))
     e2e_ms = max_over_ranks(pg, e2e_ms, dev)
     e2e = {"value": world * step_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
            "steps": args.e2e_steps,
            "copies_only_ms_per_step": min(link_ms),
            "copies_only_ms_before_after": list(link_ms),
+           "in_loop_copies": {"h2d_ms_median": loop_copy_ms[0], "d2h_ms_median": loop_copy_ms[1],
+                              "h2d_gbs": h2d / (loop_copy_ms[0] * 1e-3) / 1e9,
+                              "d2h_gbs": d2h / (loop_copy_ms[1] * 1e-3) / 1e9,
+                              "note": "each step's copies timed on their streams inside the loop; the two "
+                                      "directions overlap each other and the compute"},
            "pipelining": "copy-in of step i+1 and copy-out of step i-1 overlap step i (3 device buffer sets, "
                          "3 streams); every step's copies are inside the timed region"}
     # Window-local RoPE of q and k (a separate in-place pass, not part of the
