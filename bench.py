@@ -451,6 +451,8 @@ def full_schedule_measure(dev, steps, warmup):
     out_row_B = heads * hd * 2
     ev = lambda: torch.cuda.Event(enable_timing=True)
 
+    fused_out = schedule.output_layouts(layouts)  # the next layer's order; canonical after the last
+
     def step(variant, rec=None):
         cur = 0
         for l, lay in enumerate(layouts):
@@ -458,7 +460,7 @@ def full_schedule_measure(dev, steps, warmup):
             b = ping[cur] if variant == "qkv" else qkv[lay]
             a0, a1 = ev(), ev()
             a0.record()
-            out_layout = nxt if (variant == "fused" and nxt is not None) else vds.CANONICAL
+            out_layout = fused_out[l] if variant == "fused" else vds.CANONICAL
             vds.window_attn(plan, lay, b[:, 0], b[:, 1], b[:, 2], txt[:, 0], txt[:, 1], txt[:, 2], o_vid[0],
                             o_txt[l], ws[lay], out_layout=out_layout)
             a1.record()

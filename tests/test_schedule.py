@@ -20,3 +20,14 @@ def test_ensure_layout_is_derived_not_assumed():
     assert tr == [(REGULAR, SHIFTED), (SHIFTED, REGULAR)]
     assert schedule.ensure_layout(SHIFTED, SHIFTED) is None
     assert schedule.transitions([SHIFTED], start=REGULAR) == [(REGULAR, SHIFTED)]
+
+
+def test_output_layouts_follow_the_next_layer():
+    from video_dit_shifted_gb300 import schedule
+    lays = schedule.layer_layouts(32)
+    outs = schedule.output_layouts(lays)
+    assert len(outs) == 32
+    assert outs[:-1] == lays[1:]                      # each output in the next layer's order
+    assert outs[-1] == schedule.CANONICAL             # the last one back in canonical order
+    assert schedule.output_layouts(lays, final=schedule.REGULAR)[-1] == schedule.REGULAR
+    assert schedule.output_layouts([schedule.SHIFTED]) == [schedule.CANONICAL]

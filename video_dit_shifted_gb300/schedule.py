@@ -7,7 +7,7 @@ transitions are derived from the actual schedule with
 ensure_layout(current, required) rather than assumed from layer % 2.  The
 page leaves open which layout the first layer uses; layer 0 is regular here.
 """
-from .wp import REGULAR, SHIFTED
+from .wp import CANONICAL, REGULAR, SHIFTED
 
 
 def layer_layouts(num_layers, first=REGULAR):
@@ -30,3 +30,13 @@ def transitions(layouts, start=None):
             out.append(t)
         cur = req
     return out
+
+
+def output_layouts(layouts, final=CANONICAL):
+    """Where each layer's video attention output goes when it is written
+    straight into the next layer's order (wp_window_attn_to's out_layout):
+    the next layer's layout, and `final` (canonical order by default) after
+    the last layer.  Written this way, a schedule needs no re-layout of the
+    attention output between layers (§Plan A redistribution: at SP=1 a
+    transition is a local permutation, here folded into the epilogue)."""
+    return [layouts[l + 1] if l + 1 < len(layouts) else final for l in range(len(layouts))]
