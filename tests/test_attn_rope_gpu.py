@@ -125,7 +125,8 @@ def test_rope_attention_rotated_k_equals_rope_pass(vds, layout):
     the status block, the T_w partials and the rotated text q/k, from the
     next multiple of 1024 bytes, [N, heads, 128] bf16).  Both that pass and
     wp_rope rotate in fp32 and round once, so the copy equals wp_rope's k bit
-    for bit; k itself is left as it was.  q/k come packed with v, as a
+    for bit, and the text q/k copies equal wp_rope's text rows; k itself is
+    left as it was.  q/k come packed with v, as a
     projection writes them (row stride 3 * heads * 256 bytes)."""
     from video_dit_shifted_gb300 import synth
     grid, heads, L = (3, 30, 40, 2, 3, 3), 3, 200
@@ -146,9 +147,14 @@ def test_rope_attention_rotated_k_equals_rope_pass(vds, layout):
     assert ws.numel() == off + N * heads * 128 * 2
     krot = ws[off:].view(torch.bfloat16).view(N, heads, 128)
     ref = qkv.clone()
-    vds.rope(plan, layout, ref[:, 0], ref[:, 1], x["qt"].clone(), x["kt"].clone())
+    qt_ref, kt_ref = x["qt"].clone(), x["kt"].clone()
+    vds.rope(plan, layout, ref[:, 0], ref[:, 1], qt_ref, kt_ref)
     torch.cuda.synchronize()
     assert torch.equal(krot, ref[:, 1])
+    # the rotated text q and k, right after the T_w partials, equal wp_rope's too
+    tq = ws[plain:plain + L * heads * 256].view(torch.bfloat16).view(L, heads, 128)
+    tk = ws[plain + L * heads * 256:plain + 2 * L * heads * 256].view(torch.bfloat16).view(L, heads, 128)
+    assert torch.equal(tq, qt_ref) and torch.equal(tk, kt_ref)
     plan.close()
 
 

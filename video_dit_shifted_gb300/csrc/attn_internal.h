@@ -66,9 +66,9 @@ int static_scratch_address(void** out);
 
 // RoPE angles base^(-2i/42), i < 21, as wp_rope uses them.
 void rope_theta(float rope_base, float* theta21);
-// Copies L rows of text q and k (bf16, heads x 128 per row, row stride
-// txt_stride_B) to qt_out / kt_out (packed rows) and rotates the copies in
-// place with the text positions (l, l, l) of wp_rope.
+// Writes L rows of text q and k (bf16, heads x 128 per row, row stride
+// txt_stride_B) to qt_out / kt_out (packed rows), rotated with the text
+// positions (l, l, l) of wp_rope (the same values); qt and kt are not changed.
 int rope_text_copy(const void* qt, const void* kt, int64_t txt_stride_B, void* qt_out, void* kt_out, int L,
                    int heads, float rope_base, cudaStream_t stream);
 // Writes the N video rows of k (bf16, heads x 128 per row, layout order of

@@ -38,6 +38,8 @@ struct RopeParams {
   int64_t stride, tstride;  // bytes
   char* kdst;               // rope_k_copy_kernel: destination rows (dstride bytes apart)
   int64_t dstride;
+  char *qtdst, *ktdst;      // rope_text_copy_kernel: destination rows (tdstride bytes apart)
+  int64_t tdstride;
   const int32_t *win_off, *ids, *boxes;
   int nwin, N, L, heads, H, W;
   float theta[kPairsPerAxis];  // base^(-2i/42)
@@ -191,6 +193,32 @@ __global__ void __launch_bounds__(kWarps * 32) rope_k_copy_kernel(const RopePara
   }
 }
 
+// Text q and k rotated out of place (bf16): row l of p.qt / p.kt (stride
+// p.tstride) to row l of p.qtdst / p.ktdst (stride p.tdstride), position
+// (l, l, l); one warp per row as in rope_kernel (p.N = 0).
+__global__ void __launch_bounds__(kWarps * 32) rope_text_copy_kernel(const RopeParams p) {
+  __shared__ float2 table[kWarps][kPairs + 1];
+  const int wib = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float2* cs = table[wib];
+  constexpr int kPer = 8;
+  const int chunks = p.heads * kHd / kPer;
+  for (int64_t r = static_cast<int64_t>(blockIdx.x) * kWarps + wib; r < p.L;
+       r += static_cast<int64_t>(gridDim.x) * kWarps) {
+    row_table(p, r, cs, lane);
+    __syncwarp();
+    for (int tq = 0; tq < 2; ++tq) {
+      const char* src = (tq ? p.kt : p.qt) + r * p.tstride;
+      char* dst = (tq ? p.ktdst : p.qtdst) + r * p.tdstride;
+      for (int c = lane; c < chunks; c += 32) {
+        int4 a = __ldg(reinterpret_cast<const int4*>(src + static_cast<int64_t>(c) * 16));
+        rotate_chunk<__nv_bfloat16>(a, c, cs);
+        *reinterpret_cast<int4*>(dst + static_cast<int64_t>(c) * 16) = a;
+      }
+    }
+    __syncwarp();
+  }
+}
+
 }  // namespace
 
 void rope_theta(float rope_base, float* theta21) {
@@ -201,26 +229,20 @@ void rope_theta(float rope_base, float* theta21) {
 int rope_text_copy(const void* qt, const void* kt, int64_t txt_stride_B, void* qt_out, void* kt_out, int L,
                    int heads, float rope_base, cudaStream_t stream) {
   if (L <= 0) return WP_OK;
-  const size_t row_B = static_cast<size_t>(heads) * kHd * 2;
-  if (int rc = cuda_check(cudaMemcpy2DAsync(qt_out, row_B, qt, static_cast<size_t>(txt_stride_B), row_B, L,
-                                            cudaMemcpyDeviceToDevice, stream),
-                          "cudaMemcpy2DAsync(text q)"))
-    return rc;
-  if (int rc = cuda_check(cudaMemcpy2DAsync(kt_out, row_B, kt, static_cast<size_t>(txt_stride_B), row_B, L,
-                                            cudaMemcpyDeviceToDevice, stream),
-                          "cudaMemcpy2DAsync(text k)"))
-    return rc;
   RopeParams p{};
-  p.qt = static_cast<char*>(qt_out);
-  p.kt = static_cast<char*>(kt_out);
-  p.tstride = static_cast<int64_t>(row_B);
+  p.qt = static_cast<char*>(const_cast<void*>(qt));
+  p.kt = static_cast<char*>(const_cast<void*>(kt));
+  p.tstride = txt_stride_B;
+  p.qtdst = static_cast<char*>(qt_out);
+  p.ktdst = static_cast<char*>(kt_out);
+  p.tdstride = static_cast<int64_t>(heads) * kHd * 2;
   p.N = 0;  // text rows only: positions (l, l, l)
   p.L = L;
   p.heads = heads;
   rope_theta(rope_base, p.theta);
   const unsigned blocks = static_cast<unsigned>((L + kWarps - 1) / kWarps);
-  rope_kernel<__nv_bfloat16><<<blocks, kWarps * 32, 0, stream>>>(p);
-  return cuda_check(cudaGetLastError(), "rope_kernel launch (text)");
+  rope_text_copy_kernel<<<blocks, kWarps * 32, 0, stream>>>(p);
+  return cuda_check(cudaGetLastError(), "rope_text_copy_kernel launch");
 }
 
 int rope_k_copy(const wp_plan* plan, int layout, const void* k, int64_t vid_stride_B, void* k_out, int heads, int L,
