@@ -104,11 +104,12 @@ def test_fp8_attention_matches_oracle(vds, grid, heads, L):
         ref_o, ref_t = oa.window_attention(dq["q"], dq["k"], _np(x["v"]), dq["qt"], dq["kt"], _np(x["vt"]),
                                            off, ids)
         exact_o, exact_t = oa.window_attention(*(_np(x[n]) for n in ("q", "k", "v", "qt", "kt", "vt")), off, ids)
-        for out in (op.CANONICAL, layout):
+        other = op.SHIFTED if layout == op.REGULAR else op.REGULAR
+        for out in (op.CANONICAL, layout, other):
             o, t = _run_fp8(vds, plan, layout, x, codes, heads, L, out)
             got = _np(o)
-            if out != op.CANONICAL:        # output row r holds canonical token ids[r]
-                got = got[np.argsort(ids)]
+            if out != op.CANONICAL:        # output row r holds canonical token ids_out[r]
+                got = got[np.argsort(op.layout_tables(*grid, out)[1])]
             assert np.abs(got - ref_o).max() <= TOL, (layout, out)
             err = np.abs(got - exact_o).max()
             if L:
