@@ -639,3 +639,44 @@ def test_text_mean_is_the_ordered_fp32_mean(vds, grid, heads, hd, L):
         want = torch.from_numpy(acc / np.float32(nwin)).to(torch.bfloat16)
         assert torch.equal(o_txt.cpu(), want), layout
     plan.close()
+
+
+def _random_configs(n, seed=17):
+    import random
+    rng = random.Random(seed)
+    out = []
+    while len(out) < n:
+        grid = (rng.randint(1, 4), rng.randint(4, 40), rng.randint(4, 60),
+                rng.randint(1, 4), rng.randint(1, 4), rng.randint(1, 4))
+        if min(op.window_size(*grid)) < 1:
+            continue
+        out.append((grid, rng.randint(1, 3), rng.choice([64, 128]), rng.choice([0, 1, 7, 130]),
+                    rng.choice([torch.bfloat16, torch.float32])))
+    return out
+
+
+@pytest.mark.parametrize("grid,heads,hd,L,dtype", _random_configs(12))
+def test_random_small_configs(vds, grid, heads, hd, L, dtype):
+    """Seeded random grids, window counts, head counts, text lengths, head
+    dims and dtypes, both layouts, against the oracle (tolerances as above);
+    fp32 cases also write their output in a random layout."""
+    _check_full(vds, grid, heads, hd, L, dtype)
+    if dtype == torch.float32:
+        import random
+        from video_dit_shifted_gb300 import synth
+        out = random.Random(sum(grid)).choice([op.CANONICAL, op.REGULAR, op.SHIFTED])
+        plan = vds.Plan(*grid, device="cuda")
+        x = synth.attention_inputs(plan.N, L, heads, hd, dtype, "cuda", base_seed=31)
+        o = torch.full((plan.N, heads, hd), float("nan"), dtype=dtype, device="cuda")
+        t = torch.full((L, heads, hd), float("nan"), dtype=dtype, device="cuda")
+        ws = vds.make_workspace(plan, op.SHIFTED, heads, hd, L, vds.FP32, "cuda")
+        vds.window_attn(plan, op.SHIFTED, x["q"], x["k"], x["v"], x["qt"], x["kt"], x["vt"], o, t, ws,
+                        out_layout=out)
+        assert vds.read_status(ws) == 0
+        off, ids = op.layout_tables(*grid, op.SHIFTED)
+        ref_o, _ = oa.window_attention(*(_np(x[n]) for n in ("q", "k", "v", "qt", "kt", "vt")), off, ids)
+        got = _np(o)
+        if out != op.CANONICAL:
+            got = got[np.argsort(op.layout_tables(*grid, out)[1])]
+        assert np.abs(got - ref_o).max() <= TOL[dtype], out
+        plan.close()
