@@ -91,3 +91,34 @@ def test_sweep_full_size(vds, grid):
     assert torch.equal(back, shf[s2r])
     assert torch.equal(back, src)
     plan.close()
+
+
+def _random_cases(n, seed=23):
+    import random
+    rng = random.Random(seed)
+    out = []
+    while len(out) < n:
+        grid = (rng.randint(1, 5), rng.randint(1, 50), rng.randint(1, 70),
+                rng.randint(1, 4), rng.randint(1, 4), rng.randint(1, 4))
+        if min(op.window_size(*grid)) < 1:
+            continue
+        pair = rng.sample([op.CANONICAL, op.REGULAR, op.SHIFTED], 2)
+        out.append((grid, tuple(pair), 8 * rng.randint(1, 300)))
+    return out
+
+
+@pytest.mark.parametrize("grid,pair,width", _random_cases(10))
+def test_random_grids_bit_exact(vds, grid, pair, width):
+    """Seeded random grids, window counts, layout pairs and row widths (16 B
+    to 4.8 KB of int16): every row equals the oracle's permutation."""
+    src_l, dst_l = pair
+    plan = vds.Plan(*grid, device="cuda")
+    g = torch.Generator(device="cuda").manual_seed(sum(grid) + width)
+    src = torch.randint(-2 ** 15, 2 ** 15, (plan.N, width), dtype=torch.int16, device="cuda", generator=g)
+    dst = torch.empty_like(src)
+    vds.permute(plan, src, dst, src_l, dst_l)
+    torch.cuda.synchronize()
+    ids = {l: op.layout_tables(*grid, l)[1] for l in pair}
+    want = opm.permute_rows(src.cpu().numpy(), ids[src_l], ids[dst_l])
+    assert np.array_equal(dst.cpu().numpy(), want)
+    plan.close()

@@ -100,3 +100,38 @@ def test_rope_rejects_head_dim_64(vds):
         vds.rope(plan, op.REGULAR, q, q.clone(), None, None)
     assert e.value.code == 2
     plan.close()
+
+
+def _random_cases(n, seed=29):
+    import random
+    rng = random.Random(seed)
+    out = []
+    while len(out) < n:
+        grid = (rng.randint(1, 5), rng.randint(2, 40), rng.randint(2, 40),
+                rng.randint(1, 4), rng.randint(1, 4), rng.randint(1, 4))
+        if min(op.window_size(*grid)) < 1:
+            continue
+        out.append((grid, rng.randint(1, 3), rng.choice([0, 3, 20]),
+                    rng.choice([torch.bfloat16, torch.float32]), rng.choice([op.REGULAR, op.SHIFTED])))
+    return out
+
+
+@pytest.mark.parametrize("grid,heads,L,dtype,layout", _random_cases(8))
+def test_random_grids(vds, grid, heads, L, dtype, layout):
+    """Seeded random grids, window counts, head counts, text lengths (<= 20,
+    so positions stay within the range of the fp32 basis above), dtypes and
+    layouts, against the oracle's rotation."""
+    from video_dit_shifted_gb300 import synth
+    plan = vds.Plan(*grid, device="cuda")
+    x = synth.attention_inputs(plan.N, max(L, 1), heads, 128, dtype, "cuda", base_seed=sum(grid))
+    qt, kt = (x["qt"][:L], x["kt"][:L]) if L else (None, None)
+    before = {n: _np(x[n]) for n in ("q", "k", "qt", "kt")}
+    vds.rope(plan, layout, x["q"], x["k"], qt, kt)
+    torch.cuda.synchronize()
+    pv, pt = orp.positions(*grid, layout, L)
+    assert np.abs(_np(x["q"]) - orp.rope(before["q"], pv)).max() <= TOL[dtype]
+    assert np.abs(_np(x["k"]) - orp.rope(before["k"], pv)).max() <= TOL[dtype]
+    if L:
+        assert np.abs(_np(x["qt"][:L]) - orp.rope(before["qt"][:L], pt)).max() <= TOL[dtype]
+        assert np.abs(_np(x["kt"][:L]) - orp.rope(before["kt"][:L], pt)).max() <= TOL[dtype]
+    plan.close()
