@@ -192,3 +192,35 @@ def test_fp8_rejections(vds):
         vds.quantize_e4m3(src, torch.zeros((4, 24), dtype=torch.uint8, device="cuda"), 1.0)
     assert e.value.code == 2
     plan.close()
+
+
+def _random_cases(n, seed=41):
+    import random
+    rng = random.Random(seed)
+    out = []
+    while len(out) < n:
+        grid = (rng.randint(1, 4), rng.randint(4, 40), rng.randint(4, 60),
+                rng.randint(1, 4), rng.randint(1, 4), rng.randint(1, 4))
+        if min(op.window_size(*grid)) < 1:
+            continue
+        out.append((grid, rng.randint(1, 3), rng.choice([0, 1, 7, 130])))
+    return out
+
+
+@pytest.mark.parametrize("grid,heads,L", _random_cases(4))
+def test_fp8_random_configs(vds, grid, heads, L):
+    """Seeded random grids, window counts, head counts and text lengths: the
+    e4m3 call fed the oracle's codes against the oracle on the decoded q/k."""
+    from video_dit_shifted_gb300 import synth
+    plan = vds.Plan(*grid, device="cuda")
+    for layout in (op.REGULAR, op.SHIFTED):
+        x = synth.attention_inputs(plan.N, L, heads, 128, torch.bfloat16, "cuda", base_seed=sum(grid) + layout)
+        codes = _packed_codes(x)
+        off, ids = op.layout_tables(*grid, layout)
+        dq = {n: oq.decode(codes[n].cpu().numpy()) / INV for n in ("q", "k", "qt", "kt")}
+        ref_o, ref_t = oa.window_attention(dq["q"], dq["k"], _np(x["v"]), dq["qt"], dq["kt"], _np(x["vt"]), off, ids)
+        o, t = _run_fp8(vds, plan, layout, x, codes, heads, L)
+        assert np.abs(_np(o) - ref_o).max() <= TOL, layout
+        if L:
+            assert np.abs(_np(t) - oa.text_mean(ref_t)).max() <= TOL, layout
+    plan.close()

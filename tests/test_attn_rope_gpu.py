@@ -254,3 +254,45 @@ def test_rope_attention_1080p_sampled(vds):
     for n, b in before.items():
         assert torch.equal(x[n], b), n
     plan.close()
+
+
+def _random_cases(n, seed=37):
+    import random
+    rng = random.Random(seed)
+    out = []
+    while len(out) < n:
+        grid = (rng.randint(1, 4), rng.randint(4, 40), rng.randint(4, 60),
+                rng.randint(1, 4), rng.randint(1, 4), rng.randint(1, 4))
+        if min(op.window_size(*grid)) < 1 or sum(op.window_size(*grid)) > 196:
+            continue
+        out.append((grid, rng.randint(1, 3), rng.choice([0, 1, 7, 130]), rng.choice([op.REGULAR, op.SHIFTED]),
+                    rng.choice([op.CANONICAL, op.REGULAR, op.SHIFTED])))
+    return out
+
+
+@pytest.mark.parametrize("grid,heads,L,layout,out", _random_cases(5))
+def test_rope_attention_random_configs(vds, grid, heads, L, layout, out):
+    """Seeded random grids, window counts, head counts, text lengths, layouts
+    and output layouts, against the oracle's RoPE followed by its attention."""
+    from video_dit_shifted_gb300 import synth
+    plan = vds.Plan(*grid, device="cuda")
+    N = plan.N
+    x = synth.attention_inputs(N, max(L, 1), heads, 128, torch.bfloat16, "cuda", base_seed=sum(grid))
+    raw = {n: _np(x[n]) for n in ("q", "k", "v", "qt", "kt", "vt")}
+    if not L:
+        for n in ("qt", "kt", "vt"):
+            raw[n] = raw[n][:0]
+    o = torch.full((N, heads, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    t = torch.full((max(L, 1), heads, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ws = vds.make_workspace(plan, layout, heads, 128, L, vds.BF16, "cuda", rope=True)
+    args = (x["qt"][:L], x["kt"][:L], x["vt"][:L]) if L else (None, None, None)
+    vds.window_attn_rope(plan, layout, x["q"], x["k"], x["v"], *args, o, t[:L] if L else None, ws, out_layout=out)
+    assert vds.read_status(ws) == 0
+    ref_o, ref_t = _oracle(grid, layout, raw, L)
+    got = _np(o)
+    if out != op.CANONICAL:
+        got = got[np.argsort(op.layout_tables(*grid, out)[1])]
+    assert np.abs(got - ref_o).max() <= TOL
+    if L:
+        assert np.abs(_np(t[:L]) - ref_t).max() <= TOL
+    plan.close()
